@@ -1,0 +1,199 @@
+"""fp64 CPU oracle for causal / sliding-window GQA attention.
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it.  The product package never imports it,
+and it imports nothing from the product package.
+
+The arithmetic lives in ``attn_oracle.c`` (plain C, IEEE double); this module
+compiles it with gcc into ``oracle/_build/`` and wraps it with ctypes + numpy.
+Every function takes and returns float64 numpy arrays in the layouts
+
+    Q, O, dO, dQ : [B, T, H,   D]
+    K, V, dK, dV : [B, T, HKV, D]
+    LSE, Delta   : [B, H, T]
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, library routines, finite differences, the printed triu
+diagrams); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libattn_oracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into a shared library (gcc, -O2, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+            "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        # OpenMP only spreads rows over cores; the arithmetic is identical.
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            common = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]
+            lib.oracle_attn_probs.argtypes = [_D, _D] + common + [ctypes.c_int, ctypes.c_int, _D, _D]
+            lib.oracle_attn_fwd.argtypes = [_D, _D, _D] + common + [_D, _D]
+            lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D] + common + [_D, _D, _D, _D]
+            lib.oracle_attn_fwd_rows.argtypes = [_D, _D, _D] + common + [
+                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+            lib.oracle_attn_dq_rows.argtypes = [_D, _D, _D, _D] + common + [
+                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+            lib.oracle_attn_dkdv_rows.argtypes = [_D, _D, _D, _D] + common + [
+                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+            lib.oracle_triu_offsets.argtypes = [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]
+            for name in ("oracle_attn_probs", "oracle_attn_fwd", "oracle_attn_bwd",
+                         "oracle_attn_fwd_rows", "oracle_attn_dq_rows",
+                         "oracle_attn_dkdv_rows", "oracle_triu_offsets"):
+                getattr(lib, name).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(_D)
+
+
+def _shape(Q, K):
+    B, T, H, D = Q.shape
+    Bk, Tk, HKV, Dk = K.shape
+    if (Bk, Tk, Dk) != (B, T, D):
+        raise ValueError(f"Q {Q.shape} and K {K.shape} disagree")
+    return B, T, H, HKV, D
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise RuntimeError(f"{what} failed with status {rc}")
+
+
+def probs(Q, K, scale, causal, window, b, h):
+    """Full T x T probability matrix P of one (b, h), and its LSE row."""
+    Q, K = _f64(Q), _f64(K)
+    B, T, H, HKV, D = _shape(Q, K)
+    P = np.empty((T, T), np.float64)
+    lse = np.empty((T,), np.float64)
+    _check(_load().oracle_attn_probs(_p(Q), _p(K), B, T, H, HKV, D, float(scale),
+                                     int(causal), int(window), int(b), int(h),
+                                     _p(P), _p(lse)), "oracle_attn_probs")
+    return P, lse
+
+
+def fwd(Q, K, V, scale, causal, window):
+    """(O [B,T,H,D], LSE [B,H,T]) by the plain definition."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, T, H, HKV, D = _shape(Q, K)
+    O = np.empty_like(Q)
+    LSE = np.empty((B, H, T), np.float64)
+    _check(_load().oracle_attn_fwd(_p(Q), _p(K), _p(V), B, T, H, HKV, D, float(scale),
+                                   int(causal), int(window), _p(O), _p(LSE)),
+           "oracle_attn_fwd")
+    return O, LSE
+
+
+def bwd(Q, K, V, dO, scale, causal, window):
+    """(dQ, dK, dV, Delta) by the analytic gradient of the definition."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, T, H, HKV, D = _shape(Q, K)
+    dQ = np.empty_like(Q)
+    dK = np.empty_like(K)
+    dV = np.empty_like(V)
+    Delta = np.empty((B, H, T), np.float64)
+    _check(_load().oracle_attn_bwd(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+                                   float(scale), int(causal), int(window),
+                                   _p(dQ), _p(dK), _p(dV), _p(Delta)),
+           "oracle_attn_bwd")
+    return dQ, dK, dV, Delta
+
+
+def _rows(rows, T):
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    if r.ndim != 1 or (r.size and (r.min() < 0 or r.max() >= T)):
+        raise ValueError("row indices out of range")
+    return r
+
+
+def fwd_rows(Q, K, V, scale, causal, window, b, h, rows):
+    """O rows [n, D] and LSE [n] of query rows `rows` of one (b, h)."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    B, T, H, HKV, D = _shape(Q, K)
+    r = _rows(rows, T)
+    O = np.empty((r.size, D), np.float64)
+    L = np.empty((r.size,), np.float64)
+    _check(_load().oracle_attn_fwd_rows(_p(Q), _p(K), _p(V), B, T, H, HKV, D, float(scale),
+                                        int(causal), int(window), int(b), int(h),
+                                        r.ctypes.data_as(_I), r.size, _p(O), _p(L)),
+           "oracle_attn_fwd_rows")
+    return O, L
+
+
+def dq_rows(Q, K, V, dO, scale, causal, window, b, h, rows):
+    """dQ rows [n, D] and Delta [n] of query rows `rows` of one (b, h)."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, T, H, HKV, D = _shape(Q, K)
+    r = _rows(rows, T)
+    dq = np.empty((r.size, D), np.float64)
+    de = np.empty((r.size,), np.float64)
+    _check(_load().oracle_attn_dq_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+                                       float(scale), int(causal), int(window), int(b), int(h),
+                                       r.ctypes.data_as(_I), r.size, _p(dq), _p(de)),
+           "oracle_attn_dq_rows")
+    return dq, de
+
+
+def dkdv_rows(Q, K, V, dO, scale, causal, window, b, g, cols):
+    """dK rows and dV rows [n, D] of key rows `cols` of one (b, kv head g)."""
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, T, H, HKV, D = _shape(Q, K)
+    c = _rows(cols, T)
+    dk = np.empty((c.size, D), np.float64)
+    dv = np.empty((c.size, D), np.float64)
+    _check(_load().oracle_attn_dkdv_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+                                         float(scale), int(causal), int(window), int(b), int(g),
+                                         c.ctypes.data_as(_I), c.size, _p(dk), _p(dv)),
+           "oracle_attn_dkdv_rows")
+    return dk, dv
+
+
+def triu_offsets(num_rows: int, num_cols: int) -> list[int]:
+    """Diagonal-crossing block offsets, in the order the block walk meets them."""
+    cap = 4 * (num_rows + num_cols) + 8
+    out = (ctypes.c_int * cap)()
+    n = _load().oracle_triu_offsets(int(num_rows), int(num_cols), out, cap)
+    if n < 0 or n > cap:
+        raise RuntimeError(f"oracle_triu_offsets({num_rows}, {num_cols}) returned {n}")
+    return [out[i] for i in range(n)]

@@ -1,0 +1,481 @@
+/*
+ * attn_oracle.c -- plain fp64 CPU oracle for causal / sliding-window GQA
+ * attention, forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The product library never links, loads or calls
+ * this file.  Only the test-suite, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no source, header, table or helper with the
+ * CUDA path.
+ *
+ * What it computes is the plain definition of masked softmax attention, not
+ * the tiled online-softmax algorithm that the fused kernels use.  The online
+ * recurrence (running max m, running sum l, rescale of O, store LSE = m + log l)
+ * described in the Graphcore flash-attention-ipu page
+ * (flash_attention_qkv_packed.cpp, forward `flashAttentionQKVPackedWithStash`)
+ * and in the forge page (flash_attention.metal, header "Online softmax") is
+ * algebraically the same function, so the oracle is that function written out:
+ *
+ *   S[i][j] = scale * sum_d Q[b,i,h,d] K[b,j,g,d]         g = h / (H/HKV)
+ *   S[i][j] = -inf   where not Visible(i, j)
+ *   m_i = max_j S[i][j];  l_i = sum_j exp(S - m_i);  P = exp(S - m_i) / l_i
+ *   LSE_i = m_i + ln l_i;   O_i = sum_j P_ij V_j
+ *
+ *   Visible(i, j) <=> (!causal || j <= i) && (window == 0 || i - j < window)
+ *
+ * The visibility rule, the GQA head map g = h / (H/HKV), the [B,T,H,D]
+ * layouts, the fp32-sized LSE in [B,H,T] and the "keys kept, self included"
+ * meaning of `window` follow the forge page (flash_attention.metal: struct
+ * FlashParams and kernel flash_attn_fwd).  A row with no visible key gets
+ * O = 0 and LSE = 0, the guard of the same kernel's epilogue (it cannot occur
+ * for self-attention, where j = i is always visible).
+ *
+ * Backward (the analytic gradient of the definition above; the same formulas
+ * appear in the Graphcore page's `flashAttentionQKVPackedGrad`, the
+ * teeny-kernels page flash_attn2.rs `flash_attention2_backward_dq` /
+ * `_dkv` doc comments, and FlashMetal's flashback.metal):
+ *
+ *   dP_ij = sum_d dO[i,d] V[j,d]
+ *   Delta_i = sum_j P_ij dP_ij                  (the definition; the identity
+ *                                                Delta_i = sum_d dO_i O_i is
+ *                                                checked by the tests)
+ *   dS_ij = P_ij (dP_ij - Delta_i)
+ *   dQ_i  = scale * sum_j dS_ij K_j
+ *   dK_j  = scale * sum_{h in group g} sum_i dS_ij Q_i
+ *   dV_j  =         sum_{h in group g} sum_i P_ij dO_i
+ *
+ * All arithmetic is IEEE double, each sum taken in index order by one thread.
+ * OpenMP only spreads independent rows / columns over cores.
+ *
+ * Layouts (row-major, contiguous):
+ *   Q, O, dO, dQ : [B, T, H,   D]
+ *   K, V, dK, dV : [B, T, HKV, D]
+ *   LSE, Delta   : [B, H, T]
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_ENOMEM 2
+
+typedef struct {
+  int B, T, H, HKV, D;
+  double scale;
+  int causal, window;
+} shape_t;
+
+static int visible(const shape_t* s, long i, long j) {
+  if (s->causal && j > i) return 0;
+  if (s->window > 0 && i - j >= s->window) return 0;
+  return 1;
+}
+
+static size_t q_index(const shape_t* s, long b, long t, long h) {
+  return (((size_t)b * s->T + t) * s->H + h) * s->D;
+}
+
+static size_t kv_index(const shape_t* s, long b, long t, long g) {
+  return (((size_t)b * s->T + t) * s->HKV + g) * s->D;
+}
+
+static size_t row_index(const shape_t* s, long b, long h, long t) {
+  return ((size_t)b * s->H + h) * s->T + t;
+}
+
+static int check_shape(const shape_t* s) {
+  if (s->B < 1 || s->T < 1 || s->H < 1 || s->HKV < 1 || s->D < 1) return 0;
+  if (s->H % s->HKV != 0) return 0;
+  if (s->window < 0) return 0;
+  return 1;
+}
+
+static double dot(const double* a, const double* b, int n) {
+  double acc = 0.0;
+  for (int d = 0; d < n; ++d) acc += a[d] * b[d];
+  return acc;
+}
+
+/* One row of masked scores: S_row[j] = scale * Q_i . K_j, or -inf. */
+static void score_row(const shape_t* s, const double* Q, const double* K,
+                      long b, long h, long i, double* S_row) {
+  const long g = h / (s->H / s->HKV);
+  const double* qi = Q + q_index(s, b, i, h);
+  for (long j = 0; j < s->T; ++j) {
+    if (visible(s, i, j))
+      S_row[j] = s->scale * dot(qi, K + kv_index(s, b, j, g), s->D);
+    else
+      S_row[j] = -INFINITY;
+  }
+}
+
+/*
+ * Three-pass softmax of one score row, in place: S_row becomes P_row.
+ * Returns LSE = m + ln l, or 0 for a row with no visible key (then P_row = 0).
+ */
+static double softmax_row(double* S_row, long T) {
+  double m = -INFINITY;
+  for (long j = 0; j < T; ++j)
+    if (S_row[j] > m) m = S_row[j];
+  if (m == -INFINITY) {
+    for (long j = 0; j < T; ++j) S_row[j] = 0.0;
+    return 0.0;
+  }
+  double l = 0.0;
+  for (long j = 0; j < T; ++j) l += exp(S_row[j] - m);
+  for (long j = 0; j < T; ++j) S_row[j] = exp(S_row[j] - m) / l;
+  return m + log(l);
+}
+
+/* dP_row[j] = dO_i . V_j on visible (i, j), 0 elsewhere. */
+static void dp_row(const shape_t* s, const double* V, const double* dO,
+                   long b, long h, long i, double* dP_row) {
+  const long g = h / (s->H / s->HKV);
+  const double* doi = dO + q_index(s, b, i, h);
+  for (long j = 0; j < s->T; ++j)
+    dP_row[j] = visible(s, i, j) ? dot(doi, V + kv_index(s, b, j, g), s->D) : 0.0;
+}
+
+/* ------------------------------------------------------------------ forward */
+
+/*
+ * Full probability matrix of one (b, h): P[i*T + j].  Also LSE_head[i] if not
+ * NULL.  This is the unfused T x T matrix the flash method avoids; the oracle
+ * materialises it on purpose.
+ */
+int oracle_attn_probs(const double* Q, const double* K,
+                      int B, int T, int H, int HKV, int D,
+                      double scale, int causal, int window,
+                      int b, int h, double* P, double* LSE_head) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long i = 0; i < T; ++i) {
+    double* row = P + (size_t)i * T;
+    score_row(&s, Q, K, b, h, i, row);
+    const double lse = softmax_row(row, T);
+    if (LSE_head) LSE_head[i] = lse;
+  }
+  return ORACLE_OK;
+}
+
+/* O = P V and LSE for every (b, h), one head's T x T matrix at a time. */
+int oracle_attn_fwd(const double* Q, const double* K, const double* V,
+                    int B, int T, int H, int HKV, int D,
+                    double scale, int causal, int window,
+                    double* O, double* LSE) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s)) return ORACLE_EINVAL;
+  double* P = (double*)malloc(sizeof(double) * (size_t)T * T);
+  if (!P) return ORACLE_ENOMEM;
+  for (int b = 0; b < B; ++b) {
+    for (int h = 0; h < H; ++h) {
+      const long g = h / (H / HKV);
+      oracle_attn_probs(Q, K, B, T, H, HKV, D, scale, causal, window, b, h, P,
+                        LSE + row_index(&s, b, h, 0));
+#pragma omp parallel for schedule(dynamic, 16)
+      for (long i = 0; i < T; ++i) {
+        double* oi = O + q_index(&s, b, i, h);
+        for (int d = 0; d < D; ++d) oi[d] = 0.0;
+        for (long j = 0; j < T; ++j) {
+          const double p = P[(size_t)i * T + j];
+          if (p == 0.0) continue;
+          const double* vj = V + kv_index(&s, b, j, g);
+          for (int d = 0; d < D; ++d) oi[d] += p * vj[d];
+        }
+      }
+    }
+  }
+  free(P);
+  return ORACLE_OK;
+}
+
+/* ----------------------------------------------------------------- backward */
+
+/*
+ * dQ, dK, dV (and Delta, if not NULL) for every (b, h).  Per KV head g the
+ * rep query heads of its group are visited in order and their dK / dV
+ * contributions summed.  Materialises P and dS (T x T each) per head.
+ */
+int oracle_attn_bwd(const double* Q, const double* K, const double* V,
+                    const double* dO,
+                    int B, int T, int H, int HKV, int D,
+                    double scale, int causal, int window,
+                    double* dQ, double* dK, double* dV, double* Delta) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s)) return ORACLE_EINVAL;
+  const int rep = H / HKV;
+  double* P = (double*)malloc(sizeof(double) * (size_t)T * T);
+  double* dS = (double*)malloc(sizeof(double) * (size_t)T * T);
+  if (!P || !dS) {
+    free(P);
+    free(dS);
+    return ORACLE_ENOMEM;
+  }
+  for (int b = 0; b < B; ++b) {
+    for (int g = 0; g < HKV; ++g) {
+      for (long j = 0; j < T; ++j) {
+        memset(dK + kv_index(&s, b, j, g), 0, sizeof(double) * D);
+        memset(dV + kv_index(&s, b, j, g), 0, sizeof(double) * D);
+      }
+      for (int r = 0; r < rep; ++r) {
+        const int h = g * rep + r;
+        oracle_attn_probs(Q, K, B, T, H, HKV, D, scale, causal, window, b, h, P, NULL);
+        /* rows: dP, Delta, dS, dQ */
+#pragma omp parallel for schedule(dynamic, 16)
+        for (long i = 0; i < T; ++i) {
+          const double* Pi = P + (size_t)i * T;
+          double* dSi = dS + (size_t)i * T;
+          dp_row(&s, V, dO, b, h, i, dSi); /* dSi holds dP_i for now */
+          double delta = 0.0;
+          for (long j = 0; j < T; ++j) delta += Pi[j] * dSi[j];
+          if (Delta) Delta[row_index(&s, b, h, i)] = delta;
+          for (long j = 0; j < T; ++j) dSi[j] = Pi[j] * (dSi[j] - delta);
+          double* dqi = dQ + q_index(&s, b, i, h);
+          for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+          for (long j = 0; j < T; ++j) {
+            if (dSi[j] == 0.0) continue;
+            const double* kj = K + kv_index(&s, b, j, g);
+            for (int d = 0; d < D; ++d) dqi[d] += dSi[j] * kj[d];
+          }
+          for (int d = 0; d < D; ++d) dqi[d] *= scale;
+        }
+        /* columns: dK_j += scale * dS^T Q, dV_j += P^T dO (one thread per j) */
+#pragma omp parallel for schedule(dynamic, 16)
+        for (long j = 0; j < T; ++j) {
+          double* dkj = dK + kv_index(&s, b, j, g);
+          double* dvj = dV + kv_index(&s, b, j, g);
+          for (long i = 0; i < T; ++i) {
+            const double p = P[(size_t)i * T + j];
+            const double ds = dS[(size_t)i * T + j];
+            const double* qi = Q + q_index(&s, b, i, h);
+            const double* doi = dO + q_index(&s, b, i, h);
+            if (ds != 0.0)
+              for (int d = 0; d < D; ++d) dkj[d] += scale * ds * qi[d];
+            if (p != 0.0)
+              for (int d = 0; d < D; ++d) dvj[d] += p * doi[d];
+          }
+        }
+      }
+    }
+  }
+  free(P);
+  free(dS);
+  return ORACLE_OK;
+}
+
+/* ------------------------------------------- sampled rows (full-size checks) */
+
+/*
+ * O and LSE of selected query rows of one (b, h): O_rows[n*D + d], LSE_rows[n].
+ * Same definition as oracle_attn_fwd, evaluated only on the listed rows, so
+ * that outputs of a large problem can be checked one by one.
+ */
+int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
+                         int B, int T, int H, int HKV, int D,
+                         double scale, int causal, int window,
+                         int b, int h, const int* rows, int nrows,
+                         double* O_rows, double* LSE_rows) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
+  for (int n = 0; n < nrows; ++n)
+    if (rows[n] < 0 || rows[n] >= T) return ORACLE_EINVAL;
+  const long g = h / (H / HKV);
+  int status = ORACLE_OK;
+#pragma omp parallel
+  {
+    double* P = (double*)malloc(sizeof(double) * (size_t)T);
+    if (!P) {
+#pragma omp atomic write
+      status = ORACLE_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int n = 0; n < nrows; ++n) {
+        const long i = rows[n];
+        score_row(&s, Q, K, b, h, i, P);
+        LSE_rows[n] = softmax_row(P, T);
+        double* oi = O_rows + (size_t)n * D;
+        for (int d = 0; d < D; ++d) oi[d] = 0.0;
+        for (long j = 0; j < T; ++j) {
+          if (P[j] == 0.0) continue;
+          const double* vj = V + kv_index(&s, b, j, g);
+          for (int d = 0; d < D; ++d) oi[d] += P[j] * vj[d];
+        }
+      }
+      free(P);
+    }
+  }
+  return status;
+}
+
+/* dQ (and Delta) of selected query rows of one (b, h). */
+int oracle_attn_dq_rows(const double* Q, const double* K, const double* V,
+                        const double* dO,
+                        int B, int T, int H, int HKV, int D,
+                        double scale, int causal, int window,
+                        int b, int h, const int* rows, int nrows,
+                        double* dQ_rows, double* Delta_rows) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
+  for (int n = 0; n < nrows; ++n)
+    if (rows[n] < 0 || rows[n] >= T) return ORACLE_EINVAL;
+  const long g = h / (H / HKV);
+  int status = ORACLE_OK;
+#pragma omp parallel
+  {
+    double* P = (double*)malloc(sizeof(double) * (size_t)T);
+    double* dP = (double*)malloc(sizeof(double) * (size_t)T);
+    if (!P || !dP) {
+#pragma omp atomic write
+      status = ORACLE_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int n = 0; n < nrows; ++n) {
+        const long i = rows[n];
+        score_row(&s, Q, K, b, h, i, P);
+        softmax_row(P, T);
+        dp_row(&s, V, dO, b, h, i, dP);
+        double delta = 0.0;
+        for (long j = 0; j < T; ++j) delta += P[j] * dP[j];
+        if (Delta_rows) Delta_rows[n] = delta;
+        double* dqi = dQ_rows + (size_t)n * D;
+        for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+        for (long j = 0; j < T; ++j) {
+          const double ds = P[j] * (dP[j] - delta);
+          if (ds == 0.0) continue;
+          const double* kj = K + kv_index(&s, b, j, g);
+          for (int d = 0; d < D; ++d) dqi[d] += ds * kj[d];
+        }
+        for (int d = 0; d < D; ++d) dqi[d] *= scale;
+      }
+    }
+    free(P);
+    free(dP);
+  }
+  return status;
+}
+
+/*
+ * dK and dV of selected key rows j of one (b, g).  Every query row i of every
+ * head of the group that sees any selected j is evaluated in full (its P_i,
+ * dP_i and Delta_i), and its contribution added to the selected rows.
+ */
+int oracle_attn_dkdv_rows(const double* Q, const double* K, const double* V,
+                          const double* dO,
+                          int B, int T, int H, int HKV, int D,
+                          double scale, int causal, int window,
+                          int b, int g, const int* cols, int ncols,
+                          double* dK_rows, double* dV_rows) {
+  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  if (!check_shape(&s) || b < 0 || b >= B || g < 0 || g >= HKV) return ORACLE_EINVAL;
+  for (int n = 0; n < ncols; ++n)
+    if (cols[n] < 0 || cols[n] >= T) return ORACLE_EINVAL;
+  const int rep = H / HKV;
+  memset(dK_rows, 0, sizeof(double) * (size_t)ncols * D);
+  memset(dV_rows, 0, sizeof(double) * (size_t)ncols * D);
+  /* which query rows see at least one selected key */
+  char* need = (char*)calloc((size_t)T, 1);
+  if (!need) return ORACLE_ENOMEM;
+  for (int n = 0; n < ncols; ++n)
+    for (long i = 0; i < T; ++i)
+      if (visible(&s, i, cols[n])) need[i] = 1;
+  int status = ORACLE_OK;
+  /* Parallel over selected columns would re-evaluate rows; instead evaluate
+     each needed row once per head (in parallel) and store its P / dS values
+     at the selected columns, then reduce in row order per column. */
+  double* Psel = (double*)malloc(sizeof(double) * (size_t)T * ncols);
+  double* dSsel = (double*)malloc(sizeof(double) * (size_t)T * ncols);
+  if (!Psel || !dSsel) {
+    free(need);
+    free(Psel);
+    free(dSsel);
+    return ORACLE_ENOMEM;
+  }
+  for (int r = 0; r < rep; ++r) {
+    const int h = g * rep + r;
+#pragma omp parallel
+    {
+      double* P = (double*)malloc(sizeof(double) * (size_t)T);
+      double* dP = (double*)malloc(sizeof(double) * (size_t)T);
+      if (!P || !dP) {
+#pragma omp atomic write
+        status = ORACLE_ENOMEM;
+      } else {
+#pragma omp for schedule(dynamic, 1)
+        for (long i = 0; i < T; ++i) {
+          if (!need[i]) continue;
+          score_row(&s, Q, K, b, h, i, P);
+          softmax_row(P, T);
+          dp_row(&s, V, dO, b, h, i, dP);
+          double delta = 0.0;
+          for (long j = 0; j < T; ++j) delta += P[j] * dP[j];
+          for (int n = 0; n < ncols; ++n) {
+            const long j = cols[n];
+            Psel[(size_t)i * ncols + n] = P[j];
+            dSsel[(size_t)i * ncols + n] = P[j] * (dP[j] - delta);
+          }
+        }
+      }
+      free(P);
+      free(dP);
+    }
+    if (status != ORACLE_OK) break;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int n = 0; n < ncols; ++n) {
+      double* dkj = dK_rows + (size_t)n * D;
+      double* dvj = dV_rows + (size_t)n * D;
+      for (long i = 0; i < T; ++i) {
+        if (!need[i]) continue;
+        const double p = Psel[(size_t)i * ncols + n];
+        const double ds = dSsel[(size_t)i * ncols + n];
+        const double* qi = Q + q_index(&s, b, i, h);
+        const double* doi = dO + q_index(&s, b, i, h);
+        if (ds != 0.0)
+          for (int d = 0; d < D; ++d) dkj[d] += scale * ds * qi[d];
+        if (p != 0.0)
+          for (int d = 0; d < D; ++d) dvj[d] += p * doi[d];
+      }
+    }
+  }
+  free(need);
+  free(Psel);
+  free(dSsel);
+  return status;
+}
+
+/* ------------------------------------------------ block-offset (triu) scheme */
+
+/*
+ * The Graphcore page (flash_attention_qkv_packed.cpp, getTriuOffsetSequence
+ * and its docstring examples) splits the causal mask into blocks of
+ * numRows x numCols and keeps only the distinct diagonal-crossing blocks.
+ * Block (i, j) crosses the diagonal with offset k = i*numRows - j*numCols + 1:
+ * inside it, element (r, c) is masked iff c - r >= k.  The page walks these
+ * offsets starting from 1: each step down one block row adds numRows; when the
+ * offset passes numCols - 1 the walk moves one block column right, subtracting
+ * numRows + numCols; offsets below 2 - numRows (blocks the diagonal misses,
+ * which need no mask) are skipped, and the walk stops when it returns to 1.
+ *
+ * Writes at most `cap` offsets into `out` and returns how many the walk
+ * produced (which may exceed cap), or -1 for invalid sizes.
+ */
+int oracle_triu_offsets(int numRows, int numCols, int* out, int cap) {
+  if (numRows < 1 || numCols < 1) return -1;
+  int count = 0;
+  int k = 1;
+  const long guard = 4L * (numRows + numCols) * (numRows + numCols) + 16;
+  long steps = 0;
+  if (count < cap) out[count] = k;
+  ++count;
+  for (;;) {
+    k += numRows;
+    if (k > numCols - 1) k -= numRows + numCols;
+    if (k == 1) break;
+    if (k >= 2 - numRows) {
+      if (count < cap) out[count] = k;
+      ++count;
+    }
+    if (++steps > guard) return -1; /* the walk always returns to 1; defensive */
+  }
+  return count;
+}
