@@ -1,0 +1,267 @@
+"""ctypes binding of libfa_gb300.so (the C ABI in include/fa.h).
+
+Argument marshalling only: every attention step runs in the library's CUDA
+kernels.  The library is loaded on first use and a missing or unbuildable
+library raises immediately; there is no fallback implementation.
+
+Two layers:
+* ``fa_*`` functions with the C names and arguments (integers for pointers
+  and the stream), returning the C status code;
+* ``attention_fwd`` / ``attention_bwd`` for torch CUDA tensors, which
+  allocate outputs and the workspace with torch and raise ``FaError`` on a
+  nonzero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+FA_DTYPE_BF16 = 0
+FA_DTYPE_FP32 = 1
+FA_OP_FWD = 0
+FA_OP_BWD = 1
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)} (status {status})")
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load the library (optionally building it first); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{LIB_PATH} is not built; run `python -c \"import __graft_entry__ as g; g.build()\"` "
+                    "(there is no CPU fallback)")
+            from .build import build
+            build()
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.fa_workspace_size.argtypes = [_i] * 7
+        lib.fa_workspace_size.restype = _sz
+        lib.fa_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_fwd.restype = _i
+        lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd.restype = _i
+        lib.fa_check_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
+        lib.fa_check_status.restype = _i
+        lib.fa_status_string.argtypes = [_i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        for name in ("fa_plan_kv_range", "fa_plan_q_range"):
+            getattr(lib, name).argtypes = [_i] * 6 + [ctypes.POINTER(_i), ctypes.POINTER(_i)]
+            getattr(lib, name).restype = _i
+        lib.fa_plan_block_mask.argtypes = [_i] * 7
+        lib.fa_plan_block_mask.restype = _i
+        lib.fa_tile_m.argtypes = []
+        lib.fa_tile_m.restype = _i
+        lib.fa_tile_n.argtypes = []
+        lib.fa_tile_n.restype = _i
+        lib.fa_debug_config.argtypes = [ctypes.c_ulonglong, _i]
+        lib.fa_debug_config.restype = _i
+        _lib = lib
+        return lib
+
+
+# ------------------------------------------------------------- C-named layer
+
+def fa_workspace_size(op, B, T, H, HKV, head_dim, dtype) -> int:
+    return load().fa_workspace_size(op, B, T, H, HKV, head_dim, dtype)
+
+
+def fa_fwd(Q, K, V, O, LSE, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+           workspace, workspace_bytes, stream) -> int:
+    return load().fa_fwd(Q, K, V, O, LSE, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+                         workspace, workspace_bytes, stream)
+
+
+def fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+           workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal,
+                         window, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_check_status(workspace, stream) -> tuple[int, int]:
+    word = ctypes.c_uint(0)
+    st = load().fa_check_status(workspace, stream, ctypes.byref(word))
+    return st, word.value
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except Exception:  # library missing: still format the message
+        return f"status {status}"
+
+
+def fa_plan_kv_range(T, BM, BN, causal, window, qb):
+    lo, hi = _i(0), _i(0)
+    st = load().fa_plan_kv_range(T, BM, BN, causal, window, qb, ctypes.byref(lo), ctypes.byref(hi))
+    if st:
+        raise FaError(st, "fa_plan_kv_range")
+    return lo.value, hi.value
+
+
+def fa_plan_q_range(T, BM, BN, causal, window, kb):
+    lo, hi = _i(0), _i(0)
+    st = load().fa_plan_q_range(T, BM, BN, causal, window, kb, ctypes.byref(lo), ctypes.byref(hi))
+    if st:
+        raise FaError(st, "fa_plan_q_range")
+    return lo.value, hi.value
+
+
+def fa_plan_block_mask(T, BM, BN, causal, window, qb, kb) -> int:
+    return load().fa_plan_block_mask(T, BM, BN, causal, window, qb, kb)
+
+
+def fa_tile_m() -> int:
+    return load().fa_tile_m()
+
+
+def fa_tile_n() -> int:
+    return load().fa_tile_n()
+
+
+def fa_debug_config(wait_timeout_ns: int = 0, inject_stall: int = 0) -> int:
+    return load().fa_debug_config(int(wait_timeout_ns), int(inject_stall))
+
+
+# ------------------------------------------------------------ torch layer
+
+_ws_cache: dict = {}
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace(op: int, B, T, H, HKV, D, dtype_code, device, stream):
+    """Zero-filled workspace tensor cached per (device, stream, op, size)."""
+    torch = _torch()
+    n = fa_workspace_size(op, B, T, H, HKV, D, dtype_code)
+    if n == 0:
+        raise FaError(FA_ERR_INVALID_ARG, "fa_workspace_size")
+    key = (device.index, int(stream), op)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws, n
+
+
+def _stream(device, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream
+
+
+def attention_fwd(q, k, v, scale=None, causal=True, window=0, out=None, lse=None, stream=None):
+    """O [B,T,H,D] and LSE [B,H,T] (fp32) for q [B,T,H,D], k/v [B,T,HKV,D]."""
+    torch = _torch()
+    B, T, H, D = q.shape
+    HKV = k.shape[2]
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, T, HKV, D)), ("v", v, (B, T, HKV, D))):
+        _check_tensor(name, t, shp, q.dtype, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, T), dtype=torch.float32, device=dev) if lse is None else lse
+    _check_tensor("out", o, (B, T, H, D), q.dtype, dev)
+    _check_tensor("lse", l, (B, H, T), torch.float32, dev)
+    s = _stream(dev, stream)
+    ws, n = workspace(FA_OP_FWD, B, T, H, HKV, D, dt, dev, s)
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, T, H, HKV, D,
+                float(scale), int(bool(causal)), int(window), dt, ws.data_ptr(), n, s)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return o, l
+
+
+def attention_bwd(q, k, v, o, lse, do, scale=None, causal=True, window=0, dq=None, dk=None, dv=None,
+                  stream=None):
+    """dQ, dK, dV given the forward's O and LSE and the output gradient dO."""
+    torch = _torch()
+    B, T, H, D = q.shape
+    HKV = k.shape[2]
+    dev = q.device
+    dt = _dtype_code(q)
+    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, T, HKV, D)), ("v", v, (B, T, HKV, D)),
+                         ("o", o, (B, T, H, D)), ("do", do, (B, T, H, D))):
+        _check_tensor(name, t, shp, q.dtype, dev)
+    _check_tensor("lse", lse, (B, H, T), torch.float32, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    s = _stream(dev, stream)
+    ws, n = workspace(FA_OP_BWD, B, T, H, HKV, D, dt, dev, s)
+    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, T, H, HKV, D, float(scale),
+                int(bool(causal)), int(window), dt, ws.data_ptr(), n, s)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def check_status(device=None, stream=None, op: int = FA_OP_BWD) -> tuple[int, int]:
+    """Synchronise and read (and clear) the device error words of cached workspaces."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    s = _stream(dev, stream)
+    worst = (FA_OK, 0)
+    for (di, si, _op), ws in list(_ws_cache.items()):
+        if di == dev.index and si == s:
+            st, word = fa_check_status(ws.data_ptr(), s)
+            if st != FA_OK:
+                worst = (st, word)
+    return worst

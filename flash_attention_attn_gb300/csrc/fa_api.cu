@@ -1,0 +1,319 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// workspace layout, TMA tensor-map encoding and kernel launches.  Nothing
+// here computes attention; every arithmetic step runs in the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+using fa::Shape;
+
+constexpr size_t kErrBytes = 256;  // error word, padded to keep Delta aligned
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+std::atomic<unsigned long long> g_wait_ns{fa::kDefaultWaitNs};
+std::atomic<int> g_inject_stall{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_shape(int B, int T, int H, int HKV, int D, float scale, int causal, int window, int dtype) {
+  if (B < 1 || T < 1 || H < 1 || HKV < 1 || D < 1) return FA_ERR_INVALID_ARG;
+  if (H % HKV != 0) return FA_ERR_INVALID_ARG;
+  if (window < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || scale == INFINITY) return FA_ERR_INVALID_ARG;  // also rejects NaN
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  // grid limits (y = heads, z = batch) and 32-bit row indexing inside kernels
+  if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * T * H * D >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) + window >= (1ll << 30)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+size_t delta_bytes(int B, int T, int H) { return round_up(sizeof(float) * static_cast<size_t>(B) * H * T, 256); }
+
+// ---------------------------------------------------------------- devices
+
+struct DeviceInfo {
+  bool probed = false;
+  bool sm103 = false;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_ok(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    d.sm103 = (major == 10 && minor == 3);
+    d.probed = true;
+  }
+  *dev_out = dev;
+  return d.sm103 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return FA_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return FA_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return FA_OK;
+}
+
+// 3-D bf16 view [B][T][heads*D] of a [B,T,heads,D] tensor; boxes of 64
+// elements x 128 rows x 1 batch, 128-byte swizzle.  Rows past T of a batch
+// read as zeros.
+int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D) {
+  const cuuint64_t inner = static_cast<cuuint64_t>(heads) * D;
+  cuuint64_t dims[3] = {inner, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * static_cast<cuuint64_t>(T)};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype) {
+  if (validate_shape(B, T, H, HKV, head_dim, 1.f, 1, 0, dtype) != FA_OK) return 0;
+  if (op == FA_OP_FWD) return kErrBytes;
+  if (op == FA_OP_BWD) return kErrBytes + delta_bytes(B, T, H);
+  return 0;
+}
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int T, int H, int HKV,
+           int head_dim, float scale, int causal, int window, int dtype, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  int st = validate_shape(B, T, H, HKV, head_dim, scale, causal, window, dtype);
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < fa_workspace_size(FA_OP_FWD, B, T, H, HKV, head_dim, dtype))
+    return FA_ERR_WORKSPACE;
+  int dev;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Shape shp{B, T, H, HKV, head_dim, scale, causal, window};
+  if (dtype == FA_DTYPE_FP32)
+    return status_of(fa::launch_fwd_fp32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                         static_cast<const float*>(V), static_cast<float*>(O), LSE, shp, s));
+  if ((st = get_encoder()) != FA_OK) return st;
+  fa::TensorMaps tm;
+  if ((st = encode_map(&tm.q, Q, B, T, H, head_dim)) != FA_OK) return st;
+  if ((st = encode_map(&tm.k, K, B, T, HKV, head_dim)) != FA_OK) return st;
+  if ((st = encode_map(&tm.v, V, B, T, HKV, head_dim)) != FA_OK) return st;
+  tm.o = tm.q;
+  tm.dO = tm.q;
+  fa::FwdParams p;
+  p.s = shp;
+  p.O = O;
+  p.LSE = LSE;
+  p.err = static_cast<unsigned int*>(workspace);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = g_wait_ns.load();
+  p.inject_stall = g_inject_stall.exchange(0);
+  return status_of(fa::launch_fwd_bf16(tm, p, s));
+}
+
+namespace {
+
+// Shared checks of the backward stages; fills the shape and the Delta pointer.
+int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int H, int HKV, int head_dim, float scale,
+                 int causal, int window, int dtype, void* workspace, size_t workspace_bytes, Shape* shp,
+                 float** delta) {
+  int st = validate_shape(B, T, H, HKV, head_dim, scale, causal, window, dtype);
+  if (st != FA_OK) return st;
+  for (int i = 0; i < nptr; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i])) return FA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+      workspace_bytes < fa_workspace_size(FA_OP_BWD, B, T, H, HKV, head_dim, dtype))
+    return FA_ERR_WORKSPACE;
+  int dev;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  *shp = Shape{B, T, H, HKV, head_dim, scale, causal, window};
+  *delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + kErrBytes);
+  return FA_OK;
+}
+
+int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, const void* dO, const Shape& s) {
+  int st;
+  if ((st = get_encoder()) != FA_OK) return st;
+  if ((st = encode_map(&tm->q, Q, s.B, s.T, s.H, s.D)) != FA_OK) return st;
+  if ((st = encode_map(&tm->k, K, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
+  if ((st = encode_map(&tm->v, V, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
+  if ((st = encode_map(&tm->dO, dO, s.B, s.T, s.H, s.D)) != FA_OK) return st;
+  tm->o = tm->q;
+  return FA_OK;
+}
+
+fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, void* dQ, void* dK, void* dV,
+                         void* workspace) {
+  fa::BwdParams p;
+  p.s = s;
+  p.LSE = LSE;
+  p.Delta = delta;
+  p.dQ = dQ;
+  p.dK = dK;
+  p.dV = dV;
+  p.err = static_cast<unsigned int*>(workspace);
+  p.scale_log2 = s.scale * 1.4426950408889634f;
+  p.timeout_ns = g_wait_ns.load();
+  return p;
+}
+
+}  // namespace
+
+int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {O, dO};
+  Shape shp;
+  float* delta;
+  int st = bwd_prologue(ptrs, 2, B, T, H, HKV, head_dim, 1.f, 1, 0, dtype, workspace, workspace_bytes, &shp, &delta);
+  if (st != FA_OK) return st;
+  return status_of(fa::launch_delta(O, dO, delta, shp, dtype == FA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
+                int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {Q, K, V, LSE, dO, dK, dV};
+  Shape shp;
+  float* delta;
+  int st = bwd_prologue(ptrs, 7, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
+                        &shp, &delta);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return status_of(fa::launch_bwd_dkdv_fp32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                              static_cast<const float*>(V), static_cast<const float*>(dO), LSE,
+                                              delta, static_cast<float*>(dK), static_cast<float*>(dV), shp, s));
+  fa::TensorMaps tm;
+  if ((st = bwd_maps(&tm, Q, K, V, dO, shp)) != FA_OK) return st;
+  return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace), s));
+}
+
+int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
+              int H, int HKV, int head_dim, float scale, int causal, int window, int dtype, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  const void* ptrs[] = {Q, K, V, LSE, dO, dQ};
+  Shape shp;
+  float* delta;
+  int st = bwd_prologue(ptrs, 6, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
+                        &shp, &delta);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == FA_DTYPE_FP32)
+    return status_of(fa::launch_bwd_dq_fp32(static_cast<const float*>(Q), static_cast<const float*>(K),
+                                            static_cast<const float*>(V), static_cast<const float*>(dO), LSE, delta,
+                                            static_cast<float*>(dQ), shp, s));
+  fa::TensorMaps tm;
+  if ((st = bwd_maps(&tm, Q, K, V, dO, shp)) != FA_OK) return st;
+  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace), s));
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+           void* dK, void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
+           int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  // validate every argument before the first launch, so that a bad call
+  // launches nothing
+  const void* ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
+  Shape shp;
+  float* delta;
+  int st = bwd_prologue(ptrs, 9, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
+                        &shp, &delta);
+  if (st != FA_OK) return st;
+  if ((st = fa_bwd_preprocess(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)) != FA_OK)
+    return st;
+  if ((st = fa_bwd_dkdv(Q, K, V, LSE, dO, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                        workspace_bytes, stream)) != FA_OK)
+    return st;
+  return fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                   workspace_bytes, stream);
+}
+
+int fa_check_status(void* workspace, void* stream, unsigned int* raw_word) {
+  if (!workspace) return FA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (raw_word) *raw_word = word;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    default: return "unknown status";
+  }
+}
+
+int fa_plan_kv_range(int T, int BM, int BN, int causal, int window, int qb, int* lo, int* hi) {
+  if (T < 1 || BM < 1 || BN < 1 || window < 0 || !lo || !hi || qb < 0 || qb >= fa::ceil_div(T, BM))
+    return FA_ERR_INVALID_ARG;
+  fa::kv_range_for_q(T, BM, BN, causal, window, qb, *lo, *hi);
+  return FA_OK;
+}
+
+int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* lo, int* hi) {
+  if (T < 1 || BM < 1 || BN < 1 || window < 0 || !lo || !hi || kb < 0 || kb >= fa::ceil_div(T, BN))
+    return FA_ERR_INVALID_ARG;
+  fa::q_range_for_kv(T, BM, BN, causal, window, kb, *lo, *hi);
+  return FA_OK;
+}
+
+int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb) {
+  if (T < 1 || BM < 1 || BN < 1 || window < 0 || qb < 0 || kb < 0) return -FA_ERR_INVALID_ARG;
+  return fa::block_needs_mask(T, BM, BN, causal, window, qb, kb) ? 1 : 0;
+}
+
+int fa_tile_m(void) { return fa::kBM; }
+int fa_tile_n(void) { return fa::kBN; }
+
+int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall) {
+  g_wait_ns.store(wait_timeout_ns ? wait_timeout_ns : fa::kDefaultWaitNs);
+  g_inject_stall.store(inject_stall ? 1 : 0);
+  return FA_OK;
+}
+
+}  // extern "C"

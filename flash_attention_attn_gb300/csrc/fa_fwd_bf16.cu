@@ -1,0 +1,358 @@
+// fa_fwd_bf16.cu -- fused causal / sliding-window GQA attention forward for
+// sm_103a: TMA -> shared memory -> tcgen05 MMA -> TMEM, online softmax in
+// registers.
+//
+// One CTA computes one 128-row query tile of one (b, h).  Warp roles:
+//   warps 0-3  softmax: thread t owns query row t of the tile (= TMEM lane t).
+//   warp  4    TMA producer: the Q tile once, then K and V blocks through an
+//              NS-stage ring guarded by full/empty mbarriers.
+//   warp  5    MMA issuer (one thread) and TMEM owner.
+//
+// Per visible KV block n (the loop skips blocks above the causal diagonal and
+// before the window, and applies the per-element mask only on blocks that
+// need it):
+//   S_n = Q K_n^T          -> TMEM S[n % 2] (128 x 128 fp32)
+//   softmax: m_new = max(m, rowmax S_n); P = 2^(S*scale*log2e - m); l += rowsum P;
+//            P -> bf16 into the first 64 columns of S[n % 2]
+//   O += P V_n             -> TMEM O (128 x D fp32), A operand read from TMEM
+// S_{n+1} is computed while the softmax works on S_n.  O is rescaled only
+// when a row's max grows by more than 2^8 (the rows keep a stale reference
+// max otherwise, which is exact: numerator and denominator share it).
+// The recurrence is the online softmax of the Graphcore flash-attention-ipu
+// forward (flashAttentionQKVPackedWithStash: m_new, c = exp(m - m_new),
+// l = l*c + rowsum, o = o*c + P V, o /= l, lse = m + log l at the end).
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kChunks = D / 64;              // 64-wide bf16 chunks per row
+  static constexpr int kChunkBytes = 128 * 64 * 2;    // one [128][64] chunk
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStages = (D == 64) ? 4 : 2;   // K/V ring depth
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmS = 0;      // S[0] at 0, S[1] at 128
+  static constexpr uint32_t kTmO = 256;    // O: D columns
+};
+
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 256 between rescales
+constexpr int kThreads = 192;
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full[4];
+  uint64_t v_full[4];
+  uint64_t kv_empty[4];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Lane 0 waits, the warp follows its verdict (keeps .sync.aligned tcgen05
+// instructions convergent even when a wait gives up).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& ctl, unsigned code) {
+  bool ok = false;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, ctl, code);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
+__device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+                 "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+                 "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
+
+  const Shape& s = p.s;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nq = ceil_div(s.T, kBM);
+  const int qb = nq - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int g = h / (s.H / s.HKV);
+  int kb_lo, kb_hi;
+  kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, qb, kb_lo, kb_hi);
+  const int nblk = kb_hi - kb_lo + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 128);
+    }
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Ctl ctl{&bars->abort, p.err, p.timeout_ns};
+  constexpr unsigned kCode = 1u;  // FA_DEVERR_FWD_TIMEOUT
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !p.inject_stall) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_3d(&tmQ, &bars->q_full, smem + C::kOffQ + c * C::kChunkBytes, h * D + c * 64, qb * kBM, b);
+      int issued = 0;
+      for (int n = 0; n < nblk; ++n) {
+        const int st = n % C::kStages;
+        if (n >= C::kStages && !wait_bar(&bars->kv_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
+        const int kb = kb_lo + n;
+        uint8_t* sk = smem + C::kOffK + st * C::kTileBytes;
+        uint8_t* sv = smem + C::kOffV + st * C::kTileBytes;
+        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+        issued = n + 1;
+      }
+      if (bars->abort) {
+        // let every copy already issued land before the CTA exits
+        drain_bar(&bars->q_full, 0, p.timeout_ns);
+        for (int n = imax(0, issued - C::kStages); n < issued; ++n) {
+          drain_bar(&bars->k_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
+          drain_bar(&bars->v_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t sq = sbase + C::kOffQ;
+      bool ok = wait_bar(&bars->q_full, 0, ctl, kCode);
+      for (int n = 0; ok && n <= nblk; ++n) {
+        if (n < nblk) {
+          const int st = n % C::kStages;
+          const int sb = n & 1;
+          if (!(ok = wait_bar(&bars->k_full[st], (n / C::kStages) & 1, ctl, kCode))) break;
+          tc_fence_after();
+          const uint32_t sk = sbase + C::kOffK + st * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kTmS + sb * 128, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
+                   idesc_s, kk > 0);
+          }
+          mma_commit(&bars->s_full[sb]);
+        }
+        if (n >= 1) {
+          const int m = n - 1;
+          const int st = m % C::kStages;
+          const int sb = m & 1;
+          if (!(ok = wait_bar(&bars->p_full[sb], (m >> 1) & 1, ctl, kCode))) break;
+          if (!(ok = wait_bar(&bars->v_full[st], (m / C::kStages) & 1, ctl, kCode))) break;
+          tc_fence_after();
+          const uint32_t sv = sbase + C::kOffV + st * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            // P: 16 bf16 keys per step = 8 TMEM columns; V: 16 key rows = 2048 bytes
+            mma_ts(tmem + C::kTmO, tmem + C::kTmS + sb * 128 + kk * 8,
+                   sdesc_sw128(sv + kk * 2048, C::kChunkBytes, 1024), idesc_o, (m > 0 || kk > 0));
+          }
+          mma_commit(&bars->o_done);
+          mma_commit(&bars->kv_empty[st]);
+        }
+      }
+      // every MMA this thread issued must finish before TMEM is released
+      mma_commit(&bars->drain);
+      drain_bar(&bars->drain, 0, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = threadIdx.x;  // 0..127 = TMEM lane = tile row
+    const int row = qb * kBM + t;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    float m_run = -CUDART_INF_F;  // reference max, log2 domain
+    float l_run = 0.f;
+    bool ok = true;
+    for (int n = 0; n < nblk; ++n) {
+      const int kb = kb_lo + n;
+      const int sb = n & 1;
+      if (!(ok = warp_wait(&bars->s_full[sb], (n >> 1) & 1, ctl, kCode))) break;
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_addr + C::kTmS + sb * 128;
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(s_addr + 0, r0);
+      tmem_ld32(s_addr + 32, r1);
+      tmem_ld32(s_addr + 64, r2);
+      tmem_ld32(s_addr + 96, r3);
+      tmem_ld_wait(r0);
+      reg_tie(r1);
+      reg_tie(r2);
+      reg_tie(r3);
+      float sv[128];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        sv[c] = __uint_as_float(r0[c]);
+        sv[32 + c] = __uint_as_float(r1[c]);
+        sv[64 + c] = __uint_as_float(r2[c]);
+        sv[96 + c] = __uint_as_float(r3[c]);
+      }
+      if (block_needs_mask(s.T, kBM, kBN, s.causal, s.window, qb, kb)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (masked(s.T, s.causal, s.window, row, kb * kBN + c)) sv[c] = -CUDART_INF_F;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+      mx *= sl2;  // scale > 0, so the max commutes with the scaling
+      const float m_new = fmaxf(m_run, mx);
+      const bool first = (n == 0);
+      const bool resc = !first && (m_new - m_run > kRescaleThreshold);
+      const float m_ref = (first || resc) ? m_new : m_run;
+      const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+      float sum = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(sv[q4 * 32 + 2 * e], sl2, -m_use));
+          const float p1 = ex2(fmaf(sv[q4 * 32 + 2 * e + 1], sl2, -m_use));
+          sum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + q4 * 16, pk);
+      }
+      tmem_st_wait();
+      if (!first) {
+        if (__any_sync(0xffffffffu, resc)) {
+          // O holds P_0..P_{n-1} V; wait for the last of those MMAs, then rescale
+          if (!(ok = warp_wait(&bars->o_done, (n - 1) & 1, ctl, kCode))) break;
+          tc_fence_after();
+          const float corr = resc ? ex2(m_run - m_new) : 1.f;
+          const uint32_t o_addr = tmem + lane_addr + C::kTmO;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ro[32];
+            tmem_ld32(o_addr + c * 32, ro);
+            tmem_ld_wait(ro);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+            tmem_st32(o_addr + c * 32, ro);
+          }
+          tmem_st_wait();
+          if (resc) l_run *= corr;
+        }
+      }
+      if (first || resc) m_run = m_new;
+      l_run += sum;
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[sb]);
+    }
+    if (ok && nblk > 0) ok = warp_wait(&bars->o_done, (nblk - 1) & 1, ctl, kCode);
+    if (ok) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const uint32_t o_addr = tmem + lane_addr + C::kTmO;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ro[32];
+        tmem_ld32(o_addr + c * 32, ro);
+        tmem_ld_wait(ro);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+        if (row < s.T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row < s.T) {
+        const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : 0.f;
+        p.LSE[(static_cast<size_t>(b) * s.H + h) * s.T + row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(ceil_div(p.s.T, kBM), p.s.H, p.s.B);
+  fa_fwd_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
+  if (p.s.D == 64) return launch_fwd_d<64>(tm, p, stream);
+  if (p.s.D == 128) return launch_fwd_d<128>(tm, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -1,0 +1,116 @@
+// fa_internal.h -- declarations shared by the host library (fa_api.cu) and
+// the kernels: tile planning, kernel parameter blocks and launchers.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the encoder is fetched at run time)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// Query rows per tile and key rows per block of the bf16 tensor-core kernels.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s per pipeline wait
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
+
+// Visible(i, j) = (!causal || j <= i) && (window == 0 || i - j < window),
+// and both indices inside the sequence.
+__host__ __device__ __forceinline__ bool masked(int T, int causal, int window, int i, int j) {
+  return i >= T || j >= T || (causal && j > i) || (window > 0 && i - j >= window);
+}
+
+// KV blocks [lo, hi] that query tile qb must visit: blocks wholly above the
+// causal diagonal or wholly before the window are skipped.
+__host__ __device__ __forceinline__ void kv_range_for_q(int T, int BM, int BN, int causal, int window,
+                                                        int qb, int& lo, int& hi) {
+  const int nkv = ceil_div(T, BN);
+  const int row_lo = qb * BM;
+  const int row_hi = imin(qb * BM + BM - 1, T - 1);
+  hi = causal ? imin(nkv - 1, row_hi / BN) : nkv - 1;
+  lo = window > 0 ? imax(0, row_lo - window + 1) / BN : 0;
+}
+
+// Query tiles [lo, hi] that see any key of KV block kb.
+__host__ __device__ __forceinline__ void q_range_for_kv(int T, int BM, int BN, int causal, int window,
+                                                        int kb, int& lo, int& hi) {
+  const int nq = ceil_div(T, BM);
+  const int col_lo = kb * BN;
+  const int col_hi = imin(kb * BN + BN - 1, T - 1);
+  lo = causal ? col_lo / BM : 0;
+  hi = window > 0 ? imin(nq - 1, (col_hi + window - 1) / BM) : nq - 1;
+}
+
+// Does block (qb, kb) hold any masked element (including indices >= T)?
+// Under causal masking with BM = BN these are the diagonal blocks: the
+// block-offset k = qb*BM - kb*BN + 1 is the triu offset of that block.
+__host__ __device__ __forceinline__ bool block_needs_mask(int T, int BM, int BN, int causal, int window,
+                                                          int qb, int kb) {
+  const int row_lo = qb * BM, row_hi = qb * BM + BM - 1;
+  const int col_lo = kb * BN, col_hi = kb * BN + BN - 1;
+  if (row_hi >= T || col_hi >= T) return true;
+  if (causal && col_hi > row_lo) return true;
+  if (window > 0 && row_hi - col_lo >= window) return true;
+  return false;
+}
+
+struct Shape {
+  int B, T, H, HKV, D;
+  float scale;
+  int causal, window;
+};
+
+// ------------------------------------------------------------ bf16 kernels
+
+struct FwdParams {
+  Shape s;
+  void* O;            // bf16 [B,T,H,D]
+  float* LSE;         // [B,H,T]
+  unsigned int* err;  // device error word
+  float scale_log2;   // scale * log2(e)
+  uint64_t timeout_ns;
+  int inject_stall;
+};
+
+struct BwdParams {
+  Shape s;
+  const float* LSE;   // [B,H,T]
+  const float* Delta; // [B,H,T]
+  void* dQ;           // bf16 [B,T,H,D]
+  void* dK;           // bf16 [B,T,HKV,D]
+  void* dV;           // bf16 [B,T,HKV,D]
+  unsigned int* err;
+  float scale_log2;
+  uint64_t timeout_ns;
+};
+
+struct TensorMaps {
+  CUtensorMap q, k, v, o, dO;  // 3-D views [B][T][heads*D], box 64 x 128 x 1
+};
+
+cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------- shared kernels
+
+// Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d], fp32 accumulation.
+cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, bool bf16,
+                         cudaStream_t stream);
+
+// ----------------------------------------------------------- fp32 kernels
+
+cudaError_t launch_fwd_fp32(const float* Q, const float* K, const float* V, float* O, float* LSE,
+                            const Shape& s, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv_fp32(const float* Q, const float* K, const float* V, const float* dO,
+                                 const float* LSE, const float* Delta, float* dK, float* dV, const Shape& s,
+                                 cudaStream_t stream);
+cudaError_t launch_bwd_dq_fp32(const float* Q, const float* K, const float* V, const float* dO,
+                               const float* LSE, const float* Delta, float* dQ, const Shape& s,
+                               cudaStream_t stream);
+
+}  // namespace fa

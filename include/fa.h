@@ -1,0 +1,190 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused causal / sliding-window GQA
+ * flash-attention library (libfa_gb300.so).
+ *
+ * What it computes.  For every batch b, query head h and query row i, with
+ * KV head g = h / (H / HKV) (consecutive query heads share a KV head: forge
+ * flash_attention.metal, kernel flash_attn_fwd, the `hkv` index):
+ *
+ *   S_ij  = scale * Q[b,i,h,:] . K[b,j,g,:]
+ *   Visible(i, j) = (!causal || j <= i) && (window == 0 || i - j < window)
+ *   P_ij  = softmax_j of S_i. over visible j        (0 where not visible)
+ *   O[b,i,h,:]   = sum_j P_ij V[b,j,g,:]
+ *   LSE[b,h,i]   = log sum_j exp(S_ij)  over visible j  (natural log)
+ *
+ * `window` counts the keys a query keeps, itself included, 0 meaning no
+ * window (forge flash_attention.metal, struct FlashParams).  The forward is
+ * the online-softmax recurrence (running max m, running sum l, rescale of O,
+ * LSE = m + log l; Graphcore flash_attention_qkv_packed.cpp,
+ * flashAttentionQKVPackedWithStash) and writes nothing of size T x T.  The
+ * backward recomputes P block by block from LSE (forge flash_attention.metal,
+ * flash_attn_bwd_dq / _dv / _dk; teeny-kernels flash_attn2.rs,
+ * flash_attention2_backward_dq / _dkv):
+ *
+ *   dP_ij = dO_i . V_j ;  Delta_i = dO_i . O_i ;  dS_ij = P_ij (dP_ij - Delta_i)
+ *   dQ_i  = scale sum_j dS_ij K_j
+ *   dK_j  = scale sum_{h in group} sum_i dS_ij Q_i
+ *   dV_j  =       sum_{h in group} sum_i P_ij dO_i
+ *
+ * Layouts (all row-major and contiguous, element type `dtype` unless noted):
+ *   Q, O, dO, dQ : [B, T, H,   head_dim]
+ *   K, V, dK, dV : [B, T, HKV, head_dim]
+ *   LSE          : [B, H, T] float32 (always fp32, whatever `dtype` is)
+ *
+ * Memory and ownership.  Every pointer argument except those of
+ * fa_plan_* is a DEVICE pointer owned by the caller.  The library allocates
+ * no device memory and keeps no per-call state; it caches only the driver's
+ * tensor-map encoder and a few device attributes.  Outputs are overwritten,
+ * never accumulated into, so they need no clearing.
+ *
+ * Workspace.  Each call takes a caller-owned device workspace of at least
+ * fa_workspace_size() bytes, 256-byte aligned.  Its first 4 bytes are the
+ * device error word, which must be zero before the first call (allocate the
+ * workspace zero-filled); fa_check_status() reads it and sets it back to
+ * zero.  The backward also keeps Delta = rowsum(dO * O), [B, H, T] fp32, in
+ * the workspace.  Calls that share a workspace must be ordered (same stream).
+ *
+ * Streams.  Every launch goes onto `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and returns without synchronising.
+ *
+ * Errors.  Return values are fa_status codes.  A call that fails host-side
+ * validation returns FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED and launches
+ * nothing.  Launch failures return FA_ERR_CUDA.  Kernels never trap and never
+ * wait without bound: a pipeline wait that exceeds its time budget makes the
+ * kernel set the error word and exit, which fa_check_status() reports as
+ * FA_ERR_TIMEOUT.
+ *
+ * Supported: dtype FA_DTYPE_BF16 (tcgen05 tensor-core kernels, fp32
+ * accumulation) or FA_DTYPE_FP32 (fp32 CUDA-core kernels); head_dim 64 or
+ * 128; any B, T, H, HKV >= 1 with H % HKV == 0; scale > 0 and finite;
+ * window >= 0; 16-byte aligned tensor pointers.  No fallback path exists: an
+ * unsupported shape is an error.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad scale */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but unsupported head_dim / dtype / device */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  FA_ERR_TIMEOUT = 4,      /* a kernel wait ran out of budget (device error word) */
+  FA_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned */
+} fa_status;
+
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype;
+
+typedef enum { FA_OP_FWD = 0, FA_OP_BWD = 1 } fa_op;
+
+/*
+ * Bytes of device workspace fa_fwd (op = FA_OP_FWD) or fa_bwd (FA_OP_BWD)
+ * needs for this shape: 256 bytes for the error word, plus, for the backward,
+ * B*H*T floats of Delta (rounded up to 256 bytes).  Returns 0 for sizes that
+ * are out of range.
+ */
+size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype);
+
+/*
+ * Forward: O and LSE from Q, K, V (see the top of this file).
+ *   Q [B,T,H,D], K/V [B,T,HKV,D] in `dtype`; O [B,T,H,D] in `dtype`;
+ *   LSE [B,H,T] fp32; workspace >= fa_workspace_size(FA_OP_FWD, ...).
+ */
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+           int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
+           int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.
+ * Runs three kernels in stream order: Delta = rowsum(dO * O) into the
+ * workspace, then dK/dV (one CTA per KV block, private accumulation, no
+ * atomics), then dQ (one CTA per query block, fixed order, no atomics, so
+ * the result is bitwise reproducible).
+ *   O, LSE: exactly what fa_fwd produced for the same inputs.
+ *   workspace >= fa_workspace_size(FA_OP_BWD, ...).
+ */
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+           const void* dO, void* dQ, void* dK, void* dV,
+           int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
+           int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages of fa_bwd, callable one by one (fa_bwd runs exactly these
+ * launches, in this order, on `stream`).  Same arguments and layouts as
+ * fa_bwd; the workspace carries Delta from the first stage to the other two,
+ * so all three must get the same workspace and be stream-ordered.
+ *   fa_bwd_preprocess: Delta = rowsum(dO * O) into the workspace (HBM-bound).
+ *   fa_bwd_dkdv:       dK, dV (one CTA per KV block, no atomics).
+ *   fa_bwd_dq:         dQ (one CTA per query block, fixed order, no atomics).
+ */
+int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
+                      void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
+                int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ,
+              int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads the workspace's device error word, resets it
+ * to zero and returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a wait) or
+ * FA_ERR_CUDA (the synchronisation itself failed).  If raw_word is not NULL
+ * the word as read is stored there (bit flags, see fa_device_error_bits).
+ */
+int fa_check_status(void* workspace, void* stream, unsigned int* raw_word);
+
+/* Human-readable name of a status code (static string). */
+const char* fa_status_string(int status);
+
+/*
+ * Host mirror of the kernels' tile scheduling, exported for tests.  For tile
+ * sizes BM (query rows) x BN (key rows):
+ *   fa_plan_kv_range: the KV blocks [*lo, *hi] query tile qb must visit
+ *     (blocks wholly above the causal diagonal or wholly outside the window
+ *     are skipped);
+ *   fa_plan_q_range: the query tiles [*lo, *hi] that see KV block kb;
+ *   fa_plan_block_mask: 1 if block (qb, kb) holds any element that is
+ *     masked (not visible, or a row/key index >= T), so the per-element test
+ *     must run; 0 if every element is visible; -1 for bad sizes.
+ * The masked blocks of a causal schedule are the diagonal-crossing blocks of
+ * the Graphcore page's triu-offset scheme (getTriuOffsetSequence); inside
+ * block (qb, kb) element (r, c) is in the future iff c - r >= k with
+ * k = qb*BM - kb*BN + 1.  The range functions return FA_ERR_INVALID_ARG
+ * for bad sizes.
+ */
+int fa_plan_kv_range(int T, int BM, int BN, int causal, int window, int qb, int* lo, int* hi);
+int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* lo, int* hi);
+int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb);
+
+/* Tile sizes the bf16 kernels use (query rows, key rows per block). */
+int fa_tile_m(void);
+int fa_tile_n(void);
+
+/*
+ * Test hook.  wait_timeout_ns: budget of one pipeline wait inside a kernel
+ * (0 = the default of 2 s).  inject_stall: if nonzero, the next fa_fwd
+ * launch of the bf16 forward withholds one tile load, so that the kernel's
+ * wait runs out of budget and it exits with the device error word set; the
+ * hook clears itself after that launch.  Affects later calls of this
+ * process only.
+ */
+int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall);
+
+/* Bit flags of the device error word (which wait gave up). */
+typedef enum {
+  FA_DEVERR_FWD_TIMEOUT = 1u << 0,
+  FA_DEVERR_DKDV_TIMEOUT = 1u << 1,
+  FA_DEVERR_DQ_TIMEOUT = 1u << 2
+} fa_device_error_bits;
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,43 @@
+"""Bounded waits: a kernel whose pipeline wait runs out of budget reports it
+through the device error word and leaves the context usable.
+
+The test hook makes the next bf16 forward launch withhold its tile loads (a
+barrier that nothing completes), with a 0.2 s wait budget.  No fault, trap or
+unbounded spin is involved: the kernel's own timer ends every wait.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import flash_attention_attn_gb300 as fa
+from flash_attention_attn_gb300.inputs import Workload, as_f64, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_stalled_forward_times_out_and_recovers():
+    from flash_attention_attn_gb300.build import build
+    build()
+    w = Workload(200, "timeout", "bf16", 1, 2, 2, 256, 64, 0, True, False, "normal")
+    inp = make_inputs(w, seed=3, with_dO=False)
+    dev = torch.device("cuda", 0)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    fa.check_status()  # clear anything earlier tests left
+    try:
+        fa.fa_debug_config(200_000_000, 1)
+        fa.attention_fwd(q, k, v, causal=True)
+        st, word = fa.check_status()
+    finally:
+        fa.fa_debug_config(0, 0)
+    assert st == fa.FA_ERR_TIMEOUT
+    assert word & 1  # FA_DEVERR_FWD_TIMEOUT
+    # the context still works and the next call is correct
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, hex(word)
+    O, L = oracle.fwd(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]), w.scale, True, 0)
+    assert np.max(np.abs(o.float().cpu().numpy() - O)) <= 2e-2
+    assert np.max(np.abs(lse.cpu().numpy() - L)) <= 1e-3
