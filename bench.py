@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Attention TFLOP/s of the fused causal GQA forward + backward on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+fa_fwd, then the three backward stages (fa_bwd_preprocess, fa_bwd_dkdv,
+fa_bwd_dq), all through the C ABI on one stream, with CUDA events between
+the kernels so every kernel's duration is measured live.
+
+Counted FLOPs: 4*B*H*D*pairs for the forward and 10*B*H*D*pairs for
+forward+backward, pairs = T^2/2 under causal masking, T*W - W(W-1)/2 with a
+window.  The headline value is forward+backward TFLOP/s of the whole job.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload ID] [--shape B,H,HKV,T]
+
+Under torchrun (N > 1) every rank runs its own batch of the workload (weak
+scaling, no data-path collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd (causal GQA bf16) and % of BF16 tensor peak"
+DEFAULT_WORKLOAD = 5
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 2**20
+KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+
+
+# ------------------------------------------------------------------ counting
+
+def visible_pairs(w: Workload) -> float:
+    """Visible (query, key) pairs per head as the metric counts them."""
+    T, W = w.T, w.window
+    if not w.causal:
+        return float(T) * (min(W, T) if W else T)
+    if W and W < T:
+        return float(T) * W - W * (W - 1) / 2.0
+    return T * T / 2.0
+
+
+def counted_flops(w: Workload) -> dict:
+    base = w.B * w.H * w.D * visible_pairs(w)
+    return {"fwd": 4.0 * base, "fwd_bwd": 10.0 * base}
+
+
+def kernel_work(w: Workload, elem_bytes: int) -> dict:
+    """Algorithmic work of one launch of each kernel (flops, or bytes for the
+    HBM-bound preprocess): forward 2 matmuls per pair, dK/dV 4, dQ 3."""
+    base = w.B * w.H * w.D * visible_pairs(w)
+    rows = w.B * w.H * w.T
+    return {
+        "fwd": ("tensor", 4.0 * base),
+        "bwd_preprocess": ("hbm", 2.0 * rows * w.D * elem_bytes + 4.0 * rows),
+        "bwd_dkdv": ("tensor", 8.0 * base),
+        "bwd_dq": ("tensor", 6.0 * base),
+    }
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            out = dict(FALLBACK_PEAKS)
+            for k in out:
+                if isinstance(d.get(k), (int, float)):
+                    out[k] = float(d[k])
+            return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(name: str) -> str:
+    h = hashlib.sha256()
+    for f in (name, "sm103_ptx.cuh", "fa_internal.h"):
+        with open(os.path.join(ROOT, "flash_attention_attn_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"fwd": "fa_fwd_bf16.cu", "bwd_preprocess": "fa_delta.cu",
+                  "bwd_dkdv": "fa_bwd_bf16.cu", "bwd_dq": "fa_bwd_bf16.cu"}
+
+
+def ncu_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload with the kernel source unchanged since; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = source_sha(KERNEL_SOURCES[kernel])
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = dict(kv.split("=", 1) for kv in line.strip().split(";") if "=" in kv)
+            if parts.get("kernel") == kernel and parts.get("workload") == workload_name and parts.get("sha") == sha:
+                try:
+                    return float(parts["bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    cols = [c.strip() for c in line.split(",")]
+                    if len(cols) < 8:
+                        continue
+                    try:
+                        sm.append(float(cols[0]))
+                        mx.append(float(cols[1]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, cols[4:8]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- CPU baseline
+
+def cpu_sample_workload(w: Workload, T: int) -> Workload:
+    """One query head (and its KV head) of the workload over its first T
+    positions: same recipe and value distributions, bounded size."""
+    return w.replace(B=1, H=1, HKV=1, T=T, window=min(w.window, T) if w.window else 0)
+
+
+def cpu_sample_run(wid: int, T: int, steps: int) -> dict:
+    """Time the fp64 oracle (fwd + bwd) on the bounded sample; one run per step."""
+    import oracle
+    from flash_attention_attn_gb300.inputs import as_f64
+
+    w = cpu_sample_workload(WORKLOADS[wid], T)
+    inp = make_inputs(w)
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    oracle.build()
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.fwd(Q, K, V, w.scale, w.causal, w.window)
+        oracle.bwd(Q, K, V, dO, w.scale, w.causal, w.window)
+        times.append(time.perf_counter() - t0)
+    return {"seconds": times, "flops": counted_flops(w)["fwd_bwd"], "T": T}
+
+
+def cpu_baseline(wid: int, T: int, steps: int = 1) -> dict:
+    """Run cpu_sample_run in a fresh process with OpenMP over every core we may use."""
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OMP_PROC_BIND="false")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_sample_run(%d, %d, %d)))" % (ROOT, wid, T, steps))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(f"cpu baseline failed: {r.stderr[-2000:]}")
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["cores"] = cores
+    return d
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
+    import torch
+    import flash_attention_attn_gb300 as fa
+    from flash_attention_attn_gb300 import _binding as fb
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa.load()
+    inp = make_inputs(w, seed=w.wid + 1000 * rank)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    dt = fb.FA_DTYPE_BF16 if w.dtype == "bf16" else fb.FA_DTYPE_FP32
+    B, T, H, HKV, D = w.B, w.T, w.H, w.HKV, w.D
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, D, dt)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    s = stream.cuda_stream
+    lib = fb.load()
+    sc, causal, win = float(w.scale), int(w.causal), int(w.window)
+    P = [t.data_ptr() for t in (q, k, v, o, lse, do, dq, dk, dv)]
+    wsp = ws.data_ptr()
+
+    def check(st, what):
+        if st != 0:
+            raise fb.FaError(st, what)
+
+    def k_fwd():
+        check(lib.fa_fwd(P[0], P[1], P[2], P[3], P[4], B, T, H, HKV, D, sc, causal, win, dt, wsp, ws_bytes, s), "fa_fwd")
+
+    def k_pre():
+        check(lib.fa_bwd_preprocess(P[3], P[5], B, T, H, HKV, D, dt, wsp, ws_bytes, s), "fa_bwd_preprocess")
+
+    def k_dkdv():
+        check(lib.fa_bwd_dkdv(P[0], P[1], P[2], P[4], P[5], P[7], P[8], B, T, H, HKV, D, sc, causal, win, dt,
+                              wsp, ws_bytes, s), "fa_bwd_dkdv")
+
+    def k_dq():
+        check(lib.fa_bwd_dq(P[0], P[1], P[2], P[4], P[5], P[6], B, T, H, HKV, D, sc, causal, win, dt,
+                            wsp, ws_bytes, s), "fa_bwd_dq")
+
+    stages = (k_fwd, k_pre, k_dkdv, k_dq)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
+    flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        for f in stages:
+            f()
+    torch.cuda.synchronize(dev)
+    st, word = fb.fa_check_status(wsp, s)
+    if st != 0:
+        raise RuntimeError(f"warm-up reported device error word {word:#x}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(K):
+            if flush is not None:
+                flush.zero_()  # evict the inputs from L2 between steps (outside the events)
+            ev[i][0].record(stream)
+            for j, f in enumerate(stages):
+                f()
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    st, word = fb.fa_check_status(wsp, s)
+    if st != 0:
+        raise RuntimeError(f"timed region reported device error word {word:#x}")
+
+    per_kernel = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
+    step_ms = [ev[i][0].elapsed_time(ev[i][4]) for i in range(K)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+
+    # e2e: host buffers in pinned memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        h_in = [t.cpu().pin_memory() for t in (inp["q"], inp["k"], inp["v"], inp["do"])]
+        d_in = (q, k, v, do)
+        outs = (o, lse, dq, dk, dv)
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        e2e_steps = max(2, min(K, 5))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for hsrc, ddst in zip(h_in, d_in):
+                ddst.copy_(hsrc, non_blocking=True)
+            for f in stages:
+                f()
+            for dsrc, hdst in zip(outs, h_out):
+                hdst.copy_(dsrc, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+        e2e = {"value": world * e2e_steps * counted_flops(w)["fwd_bwd"] / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "ms_per_step": 1e3 * e2e_s / e2e_steps}
+
+    return {"per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
+            "e2e": e2e, "elem_bytes": q.element_size()}
+
+
+def workload_from_args(args) -> Workload:
+    w = WORKLOADS[args.workload]
+    if args.shape:
+        B, H, HKV, T = (int(x) for x in args.shape.split(","))
+        w = w.replace(B=B, H=H, HKV=HKV, T=T, name=f"{w.name} [reduced to B{B} H{H}/{HKV} T{T}]")
+    return w
+
+
+def config_of(w: Workload, l2_note: str) -> dict:
+    return {"workload": w.name, "B": w.B, "H": w.H, "HKV": w.HKV, "T": w.T, "head_dim": w.D,
+            "window": w.window, "causal": w.causal, "scale": w.scale, "input_recipe": w.recipe,
+            "flops_per_step_fwd_bwd": counted_flops(w)["fwd_bwd"],
+            "flop_count": "fwd 4*B*H*D*pairs, fwd+bwd 10*B*H*D*pairs; pairs = T^2/2 causal, T*W - W(W-1)/2 windowed",
+            "l2": l2_note}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--shape", default=None, help="B,H,HKV,T: reduced size of the same workload (profiling)")
+    ap.add_argument("--cpu-T", type=int, default=16384, help="sequence prefix of the CPU-baseline sample")
+    ap.add_argument("--ref-T", type=int, default=4096, help="sequence prefix per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not args.shape:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    w = workload_from_args(args)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # the reference arm is the fp64 oracle on the host cores, rank 0 only
+        if rank != 0:
+            return
+        s = cpu_baseline(w.wid, args.ref_T, steps=args.warmup + args.steps)
+        times = s["seconds"][args.warmup:]
+        tot = sum(times)
+        val = len(times) * s["flops"] / tot / 1e12
+        sample = (f"fp64 oracle fwd+bwd of one query head of '{w.name}' over its first "
+                  f"{args.ref_T} positions per step ({s['flops'] / 1e9:.1f} GFLOP counted)")
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config_of(w, "host run; no GPU"),
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": s["cores"], "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    # CPU baseline first (a fresh process, before this one touches the GPU)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w.wid, args.cpu_T, steps=1)
+
+    world, rank, local = dist_setup(args)
+    r = run_ours(args, w, world, rank, local)
+    if rank != 0:
+        return
+    import torch
+
+    peaks, peak_src = load_peaks()
+    flops = counted_flops(w)
+    work = kernel_work(w, r["elem_bytes"])
+    value = world * args.steps * flops["fwd_bwd"] / r["total_s"] / 1e12
+    kern = {}
+    for name in KERNELS:
+        ms = statistics.mean(r["per_kernel_ms"][name])
+        bound, amount = work[name]
+        if bound == "tensor":
+            peak = peaks["bf16_tflops_sustained"]
+            achieved = amount / (ms / 1e3) / 1e12
+            unit = "TFLOP/s"
+        else:
+            peak = peaks["hbm_gbs"]
+            achieved = amount / (ms / 1e3) / 1e9
+            unit = "GB/s"
+        kern[name] = {"ms": ms, "bound": bound, "achieved": achieved, "unit": unit, "peak": peak,
+                      "frac": achieved / peak, "work_per_launch": amount}
+    dom = max(KERNELS, key=lambda n: kern[n]["ms"])
+    traffic = ncu_traffic(dom, w.name)
+    roof = {"bound": kern[dom]["bound"], "achieved": kern[dom]["achieved"], "peak": kern[dom]["peak"],
+            "unit": kern[dom]["unit"], "frac": kern[dom]["frac"], "traffic": traffic, "kernel": dom,
+            "work_per_launch": kern[dom]["work_per_launch"],
+            "peak_source": f"{peak_src} ({'sustained bf16' if kern[dom]['bound'] == 'tensor' else 'HBM copy'})"}
+    fwd_ms = statistics.mean(r["per_kernel_ms"]["fwd"])
+    in_bytes = w.B * w.T * (2 * w.H + 2 * w.HKV) * w.D * r["elem_bytes"]
+    l2_note = ("inputs larger than L2 (no flush)" if in_bytes > L2_BYTES
+               else "L2 flushed between steps (256 MiB write, outside the events)")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": statistics.mean(r["step_ms"]),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": config_of(w, l2_note),
+        "fwd_tflops": flops["fwd"] / (fwd_ms / 1e3) / 1e12,
+        "fwd_pct_of_peak": 100.0 * flops["fwd"] / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "fwd_bwd_pct_of_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+        "fwd_bwd_tflops_x14": 14.0 / 10.0 * value,
+        "peak_bf16_tflops": peaks["bf16_tflops_sustained"],
+        "peak_source": peak_src,
+        "roofline": roof,
+        "kernels": kern,
+        "gpu_launches": 4 * args.steps,
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+        "device": torch.cuda.get_device_name(0),
+    }
+    if cpu is not None:
+        t = cpu["seconds"][0]
+        line["cpu_baseline"] = {
+            "value": cpu["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": cpu["cores"], "kind": "oracle",
+            "seconds": t,
+            "sample": (f"fp64 oracle fwd+bwd of one query head of '{w.name}' over its first {cpu['T']} "
+                       f"positions ({cpu['flops'] / 1e9:.1f} GFLOP counted)")}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

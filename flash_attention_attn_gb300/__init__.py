@@ -21,6 +21,9 @@ from ._binding import (  # noqa: F401
     attention_fwd,
     check_status,
     fa_bwd,
+    fa_bwd_dkdv,
+    fa_bwd_dq,
+    fa_bwd_preprocess,
     fa_check_status,
     fa_debug_config,
     fa_fwd,

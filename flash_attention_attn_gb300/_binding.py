@@ -67,6 +67,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_fwd.restype = _i
         lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd.restype = _i
+        lib.fa_bwd_preprocess.argtypes = [_vp, _vp] + [_i] * 6 + [_vp, _sz, _vp]
+        lib.fa_bwd_preprocess.restype = _i
+        lib.fa_bwd_dkdv.argtypes = [_vp] * 7 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_dkdv.restype = _i
+        lib.fa_bwd_dq.argtypes = [_vp] * 6 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_dq.restype = _i
         lib.fa_check_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
         lib.fa_check_status.restype = _i
         lib.fa_status_string.argtypes = [_i]
@@ -102,6 +108,22 @@ def fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causa
            workspace, workspace_bytes, stream) -> int:
     return load().fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal,
                          window, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_preprocess(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_preprocess(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_dkdv(Q, K, V, LSE, dO, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+                workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_dkdv(Q, K, V, LSE, dO, dK, dV, B, T, H, HKV, head_dim, scale, causal, window,
+                              dtype, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+              workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+                            workspace, workspace_bytes, stream)
 
 
 def fa_check_status(workspace, stream) -> tuple[int, int]:
