@@ -132,6 +132,46 @@ int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, con
               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd_static_scratch: fa_bwd for callers that cannot allocate device
+ * memory.  The source pages have no counterpart of this entry point; it
+ * exists for the library's users.
+ *
+ * Who needs it: code that may not call cudaMalloc (or any allocating
+ * routine) at the point where it runs the backward -- for example inside
+ * another allocator's callback, in a plugin whose host program owns every
+ * device allocation, or on a path that must not touch the allocator while a
+ * CUDA graph is being built.  fa_bwd's workspace (the Delta rows and the
+ * error word) is then out of reach, so this variant keeps that scratch in a
+ * fixed device array inside the library itself.
+ *
+ *   Inputs and outputs: exactly those of fa_bwd, caller-owned device memory.
+ *   Scratch: a static device array of 256 bytes plus
+ *     FA_STATIC_SCRATCH_MAX_ROWS floats (16 MiB + 256 B).  Every GPU that
+ *     loads the library holds these bytes until the process exits.
+ *   Limit: B*H*T <= FA_STATIC_SCRATCH_MAX_ROWS; larger shapes return
+ *     FA_ERR_WORKSPACE before anything is launched.
+ *   err_word: optional caller-owned device pointer (4-byte aligned) that
+ *     receives this call's device error word (0, or fa_device_error_bits
+ *     when a kernel wait ran out of budget); NULL to skip.
+ *   No allocation: the call makes no cudaMalloc/cudaFree or other allocating
+ *     call; it only issues a 4-byte memset (clearing the error word, since
+ *     the array keeps the previous call's contents), the three backward
+ *     kernels, and, with err_word, a 4-byte device-to-device copy.
+ *   Set-up: the first call on each device looks the array's device address
+ *     up with that device current (cudaGetSymbolAddress); make that first
+ *     call before any stream capture.
+ *   Sharing: all calls share the one array per device, so calls whose work
+ *     overlaps on the GPU (different streams, or threads racing on one
+ *     device) race on it; order them on one stream.
+ * Returns the same status codes as fa_bwd.
+ */
+#define FA_STATIC_SCRATCH_MAX_ROWS (4 * 1024 * 1024)
+int fa_bwd_static_scratch(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                          const void* dO, void* dQ, void* dK, void* dV,
+                          int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
+                          int dtype, unsigned int* err_word, void* stream);
+
+/*
  * Synchronises `stream`, reads the workspace's device error word, resets it
  * to zero and returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up on a wait) or
  * FA_ERR_CUDA (the synchronisation itself failed).  If raw_word is not NULL
