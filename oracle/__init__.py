@@ -56,28 +56,64 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    common = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attn_probs.argtypes = [_D, _D] + common + [ctypes.c_int, ctypes.c_int, _D, _D]
+    lib.oracle_attn_fwd.argtypes = [_D, _D, _D] + common + [_D, _D]
+    lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D] + common + [_D, _D, _D, _D]
+    lib.oracle_attn_fwd_rows.argtypes = [_D, _D, _D] + common + [
+        ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+    lib.oracle_attn_dq_rows.argtypes = [_D, _D, _D, _D] + common + [
+        ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+    lib.oracle_attn_dkdv_rows.argtypes = [_D, _D, _D, _D] + common + [
+        ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
+    lib.oracle_triu_offsets.argtypes = [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]
+    for name in ("oracle_attn_probs", "oracle_attn_fwd", "oracle_attn_bwd",
+                 "oracle_attn_fwd_rows", "oracle_attn_dq_rows",
+                 "oracle_attn_dkdv_rows", "oracle_triu_offsets"):
+        getattr(lib, name).restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            common = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]
-            lib.oracle_attn_probs.argtypes = [_D, _D] + common + [ctypes.c_int, ctypes.c_int, _D, _D]
-            lib.oracle_attn_fwd.argtypes = [_D, _D, _D] + common + [_D, _D]
-            lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D] + common + [_D, _D, _D, _D]
-            lib.oracle_attn_fwd_rows.argtypes = [_D, _D, _D] + common + [
-                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
-            lib.oracle_attn_dq_rows.argtypes = [_D, _D, _D, _D] + common + [
-                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
-            lib.oracle_attn_dkdv_rows.argtypes = [_D, _D, _D, _D] + common + [
-                ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
-            lib.oracle_triu_offsets.argtypes = [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]
-            for name in ("oracle_attn_probs", "oracle_attn_fwd", "oracle_attn_bwd",
-                         "oracle_attn_fwd_rows", "oracle_attn_dq_rows",
-                         "oracle_attn_dkdv_rows", "oracle_triu_offsets"):
-                getattr(lib, name).restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def compile_variant(src: str, out_path: str) -> None:
+    """Compile C source text (the oracle with a planted mistake, in the
+    mutation tests) into a shared library at out_path."""
+    src_path = out_path + ".c"
+    with open(src_path, "w") as f:
+        f.write(src)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    src_path, "-o", out_path, "-lm"], check=True, capture_output=True, text=True)
+
+
+class use_library:
+    """Context manager: route every function of this module to another build
+    of the oracle (used only by the mutation tests)."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self._saved = _load()
+        _lib = _bind(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _f64(a) -> np.ndarray:

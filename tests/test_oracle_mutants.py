@@ -1,0 +1,183 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong sign, index or head map, a transposed operand, an off-by-one
+mask), builds that copy into its own library on the CPU, and runs a battery
+of the independent pins (torch float64 SDPA + autograd, finite differences,
+closed forms, the printed triu walk) against it.  Every mutant must fail at
+least one pin; the unmodified oracle must pass them all.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _visible(T, causal, window):
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    v = np.ones((T, T), bool)
+    if causal:
+        v &= j <= i
+    if window:
+        v &= (i - j) < window
+    return v
+
+
+def _sdpa(Q, K, V, dO, scale, causal, window):
+    q, k, v = (torch.tensor(x).permute(0, 2, 1, 3).requires_grad_(True) for x in (Q, K, V))
+    mask = torch.tensor(_visible(Q.shape[1], causal, window))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask, scale=scale, enable_gqa=True)
+    o.backward(torch.tensor(dO).permute(0, 2, 1, 3))
+    return o.detach().permute(0, 2, 1, 3).numpy(), [t.grad.permute(0, 2, 1, 3).numpy() for t in (q, k, v)]
+
+
+def _pin_sdpa():
+    rng = np.random.default_rng(5)
+    for (B, T, H, HKV, D, causal, W) in ((1, 9, 4, 2, 5, True, 3), (2, 7, 2, 1, 4, False, 0), (1, 11, 6, 3, 4, True, 0)):
+        Q, K, V, dO = (rng.standard_normal(s) for s in ((B, T, H, D), (B, T, HKV, D), (B, T, HKV, D), (B, T, H, D)))
+        sc = 0.6
+        O, LSE = oracle.fwd(Q, K, V, sc, causal, W)
+        dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, causal, W)
+        Or, (dQr, dKr, dVr) = _sdpa(Q, K, V, dO, sc, causal, W)
+        for a, r in ((O, Or), (dQ, dQr), (dK, dKr), (dV, dVr)):
+            if not np.allclose(a, r, rtol=0, atol=1e-10):
+                return False
+        # LSE against the log-sum-exp of the masked scores
+        rep = H // HKV
+        vis = _visible(T, causal, W)
+        for h in range(H):
+            S = sc * np.einsum("id,jd->ij", Q[0, :, h], K[0, :, h // rep])
+            want = np.array([np.log(np.sum(np.exp(S[i, vis[i]]))) for i in range(T)])
+            if not np.allclose(LSE[0, h], want, rtol=0, atol=1e-10):
+                return False
+    return True
+
+
+def _pin_rows_match_full():
+    rng = np.random.default_rng(6)
+    B, T, H, HKV, D = 1, 10, 4, 2, 3
+    Q, K, V, dO = (rng.standard_normal(s) for s in ((B, T, H, D), (B, T, HKV, D), (B, T, HKV, D), (B, T, H, D)))
+    O, LSE = oracle.fwd(Q, K, V, 0.5, True, 4)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, 0.5, True, 4)
+    rows = [0, 3, 9]
+    for h in range(H):
+        o, l = oracle.fwd_rows(Q, K, V, 0.5, True, 4, 0, h, rows)
+        dq, _ = oracle.dq_rows(Q, K, V, dO, 0.5, True, 4, 0, h, rows)
+        if not (np.allclose(o, O[0, rows, h], atol=1e-12) and np.allclose(l, LSE[0, h, rows], atol=1e-12)
+                and np.allclose(dq, dQ[0, rows, h], atol=1e-12)):
+            return False
+    for g in range(HKV):
+        dk, dv = oracle.dkdv_rows(Q, K, V, dO, 0.5, True, 4, 0, g, rows)
+        if not (np.allclose(dk, dK[0, rows, g], atol=1e-12) and np.allclose(dv, dV[0, rows, g], atol=1e-12)):
+            return False
+    return True
+
+
+def _pin_triu():
+    """The walk's offsets: the hand-derived sequences of the printed examples,
+    and the closed form k = i*bq - j*bkv + 1 over the blocks that need a mask,
+    in visit order, for every block shape up to 8 x 8."""
+    try:
+        if not (oracle.triu_offsets(2, 2) == [1] and oracle.triu_offsets(2, 3) == [1, 0, 2]
+                and oracle.triu_offsets(2, 4) == [1, 3]):
+            return False
+        for bq in range(1, 9):
+            for bkv in range(2, 9):
+                n = int(np.lcm(bq, bkv)) * 3
+                closed = [i * bq - j * bkv + 1 for i in range(n // bq) for j in range(n // bkv)
+                          if (i + 1) * bq > j * bkv and i * bq < (j + 1) * bkv - 1]
+                walk = oracle.triu_offsets(bq, bkv)
+                if [walk[c % len(walk)] for c in range(len(closed))] != closed:
+                    return False
+        return True
+    except RuntimeError:
+        return False
+
+
+def _pin_finite_differences():
+    rng = np.random.default_rng(7)
+    Q, K, V, dO = (rng.standard_normal(s) for s in ((1, 4, 2, 2), (1, 4, 1, 2), (1, 4, 1, 2), (1, 4, 2, 2)))
+    sc, causal, W = 0.8, True, 3
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, sc, causal, W)
+
+    def loss(q, k, v):
+        return float(np.sum(oracle.fwd(q, k, v, sc, causal, W)[0] * dO))
+
+    h = 1e-6
+    for X, G, which in ((Q, dQ, 0), (K, dK, 1), (V, dV, 2)):
+        for idx in np.ndindex(X.shape):
+            args_p = [Q.copy(), K.copy(), V.copy()]
+            args_m = [Q.copy(), K.copy(), V.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            if abs(fd - G[idx]) > 1e-6 * max(1.0, abs(G[idx])):
+                return False
+    return True
+
+
+PINS = {"sdpa+lse": _pin_sdpa, "rows": _pin_rows_match_full, "triu": _pin_triu, "fd": _pin_finite_differences}
+
+
+def _failing_pins():
+    failed = []
+    for name, pin in PINS.items():
+        try:
+            ok = pin()
+        except Exception:
+            ok = False
+        if not ok:
+            failed.append(name)
+    return failed
+
+
+# (name, text in attn_oracle.c, replacement, which occurrence to replace)
+MUTANTS = [
+    ("score scale dropped", "S_row[j] = s->scale * dot(", "S_row[j] = dot(", 0),
+    ("GQA map h % HKV", "const long g = h / (s->H / s->HKV);\n  const double* qi", "const long g = h % s->HKV;\n  const double* qi", 0),
+    ("window off by one", "i - j >= s->window) return 0;", "i - j > s->window) return 0;", 0),
+    ("causal drops diagonal", "if (s->causal && j > i) return 0;", "if (s->causal && j >= i) return 0;", 0),
+    ("softmax not normalised", "S_row[j] = exp(S_row[j] - m) / l;", "S_row[j] = exp(S_row[j] - m);", 0),
+    ("LSE without log", "return m + log(l);", "return m + l;", 0),
+    ("Delta term dropped", "dSi[j] = Pi[j] * (dSi[j] - delta);", "dSi[j] = Pi[j] * dSi[j];", 0),
+    ("dS sign flipped", "dSi[j] = Pi[j] * (dSi[j] - delta);", "dSi[j] = Pi[j] * (delta - dSi[j]);", 0),
+    ("dQ without scale", "for (int d = 0; d < D; ++d) dqi[d] *= scale;", "", 0),
+    ("dQ uses V", "const double* kj = K + kv_index(&s, b, j, g);\n            for (int d = 0; d < D; ++d) dqi[d]",
+     "const double* kj = V + kv_index(&s, b, j, g);\n            for (int d = 0; d < D; ++d) dqi[d]", 0),
+    ("dK without scale", "dkj[d] += scale * ds * qi[d];", "dkj[d] += ds * qi[d];", 0),
+    ("dV from dS", "for (int d = 0; d < D; ++d) dvj[d] += p * doi[d];", "for (int d = 0; d < D; ++d) dvj[d] += ds * doi[d];", 0),
+    ("P transposed in dK/dV", "const double p = P[(size_t)i * T + j];", "const double p = P[(size_t)j * T + i];", 0),
+    ("dP reads the wrong V row", "dot(doi, V + kv_index(s, b, j, g), s->D)", "dot(doi, V + kv_index(s, b, i, g), s->D)", 0),
+    ("triu wrap too small", "if (k > numCols - 1) k -= numRows + numCols;", "if (k > numCols - 1) k -= numCols;", 0),
+    ("row LSE missing in dq rows", "softmax_row(P, T);\n        dp_row(&s, V, dO, b, h, i, dP);\n        double delta",
+     "dp_row(&s, V, dO, b, h, i, dP);\n        double delta", 0),
+]
+
+
+def _replace_nth(text, old, new, n):
+    pos = -1
+    for _ in range(n + 1):
+        pos = text.find(old, pos + 1)
+        if pos < 0:
+            raise AssertionError(f"mutation anchor not found: {old!r}")
+    return text[:pos] + new + text[pos + len(old):]
+
+
+def test_unmodified_oracle_passes_the_battery():
+    assert _failing_pins() == []
+
+
+@pytest.mark.parametrize("name,old,new,nth", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new, nth):
+    src = _replace_nth(oracle.source(), old, new, nth)
+    lib = os.path.join(tmp_path, "libmutant.so")
+    oracle.compile_variant(src, lib)
+    with oracle.use_library(lib):
+        failed = _failing_pins()
+    assert failed, f"mutant '{name}' passed every pin"
