@@ -83,13 +83,13 @@ int get_encoder() {
 }
 
 // 3-D bf16 view [B][T][heads*D] of a [B,T,heads,D] tensor; boxes of 64
-// elements x 128 rows x 1 batch, 128-byte swizzle.  Rows past T of a batch
-// read as zeros.
-int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D) {
+// elements x box_rows rows x 1 batch, 128-byte swizzle.  Rows past T of a
+// batch read as zeros.
+int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D, int box_rows = 128) {
   const cuuint64_t inner = static_cast<cuuint64_t>(heads) * D;
   cuuint64_t dims[3] = {inner, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[2] = {inner * 2, inner * 2 * static_cast<cuuint64_t>(T)};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -132,8 +132,6 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if ((st = encode_map(&tm.q, Q, B, T, H, head_dim)) != FA_OK) return st;
   if ((st = encode_map(&tm.k, K, B, T, HKV, head_dim)) != FA_OK) return st;
   if ((st = encode_map(&tm.v, V, B, T, HKV, head_dim)) != FA_OK) return st;
-  tm.o = tm.q;
-  tm.dO = tm.q;
   fa::FwdParams p;
   p.s = shp;
   p.O = O;
@@ -172,7 +170,10 @@ int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, co
   if ((st = encode_map(&tm->k, K, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
   if ((st = encode_map(&tm->v, V, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
   if ((st = encode_map(&tm->dO, dO, s.B, s.T, s.H, s.D)) != FA_OK) return st;
-  tm->o = tm->q;
+  if ((st = encode_map(&tm->q64, Q, s.B, s.T, s.H, s.D, 64)) != FA_OK) return st;
+  if ((st = encode_map(&tm->k64, K, s.B, s.T, s.HKV, s.D, 64)) != FA_OK) return st;
+  if ((st = encode_map(&tm->v64, V, s.B, s.T, s.HKV, s.D, 64)) != FA_OK) return st;
+  if ((st = encode_map(&tm->dO64, dO, s.B, s.T, s.H, s.D, 64)) != FA_OK) return st;
   return FA_OK;
 }
 

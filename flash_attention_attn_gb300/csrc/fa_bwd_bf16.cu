@@ -2,32 +2,39 @@
 //
 // Two kernels, each recomputing P block by block from the forward's LSE:
 //
-// dK/dV: one CTA per (b, kv head g, 128-row KV block).  It keeps K and V in
-//   shared memory and dK, dV in TMEM for its whole life, and visits every
-//   query head of the group and every 128-row query block that sees the KV
-//   block.  Accumulation is private to the CTA: no atomics.
+// dK/dV: one CTA per (b, kv head g, 128-row KV block).  K and V stay in
+//   shared memory and dK, dV in TMEM for the CTA's whole life while it visits
+//   every query head of the group and every 64-row query block that sees the
+//   KV block.  Accumulation is private to the CTA: no atomics.
 //     S^T  = K Q^T          (TMEM, KV rows on lanes)
 //     dP^T = V dO^T
 //     P^T  = 2^(S^T*scale*log2e - LSE*log2e), masked           -> bf16, TMEM
-//     dV  += P^T dO          (A operand from TMEM)
 //     dS^T = P^T (dP^T - Delta)                                -> bf16, TMEM
-//     dK  += dS^T Q
+//     dV  += P^T dO ;  dK += dS^T Q   (A operands from TMEM)
 //   and at the end dK *= scale.  (forge flash_attention.metal,
 //   flash_attn_bwd_dv / flash_attn_bwd_dk: one owner per key row summing over
 //   the group's query heads; teeny-kernels flash_attn2.rs,
 //   flash_attention2_backward_dkv: no atomics are needed.)
 //
-// dQ: one CTA per (b, h, 128-row query block); loops over the visible KV
-//   blocks in a fixed order, so the result is bitwise reproducible.
+// dQ: one CTA per (b, h, 128-row query block); loops over the visible 64-row
+//   KV blocks in a fixed order, so the result is bitwise reproducible.
 //     S = Q K^T ; dP = dO V^T ; dS = P (dP - Delta) -> bf16, TMEM ; dQ += dS K
 //   and at the end dQ *= scale.  (forge flash_attention.metal,
 //   flash_attn_bwd_dq; teeny-kernels flash_attention2_backward_dq.)
 //
+// Pipelining: the score and dP tiles are 64 columns wide and double-buffered
+// in TMEM, so the MMA warp computes block n+1's S and dP while the compute
+// warps work on block n.  The compute warps load S and dP of a block
+// together, produce P and dS in one pass, store them and signal once; the
+// MMA warp then queues the accumulator MMAs of the block.  The per-row LSE
+// and Delta of each streamed query block travel with its stage (the
+// producer warp loads them next to the TMA copies).
+//
 // Warp roles in both kernels: warps 0-7 compute (warp w owns TMEM lanes
-// 32*(w%4).. and the column half w/4), warp 8 TMA producer, warp 9 MMA issuer
-// and TMEM owner.  Both compute halves write their bf16 results back into the
-// columns they themselves read, so no half overwrites data the other half
-// still has to load.
+// 32*(w%4).. and the 32-column half w/4 of each 64-column tile), warp 8 TMA
+// producer, warp 9 MMA issuer and TMEM owner.  Each half writes its bf16
+// results back into the first 16 columns of the 32 it read, so no half
+// overwrites data the other still has to load.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -41,7 +48,9 @@ using namespace ptx;
 
 constexpr int kThreads = 320;
 constexpr int kCompute = 256;
+constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kRowBytes = 128;  // one 64-element bf16 row of a swizzled chunk
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& ctl, unsigned code) {
   bool ok = false;
@@ -60,37 +69,31 @@ __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-// Named barrier over the 256 compute threads (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// TMEM column of the 16-wide K slice kk (0..3) of a 64-wide bf16 operand that
+// the two compute halves wrote: half 0 packs elements 0..31 into columns
+// [0, 16), half 1 packs elements 32..63 into columns [32, 48).
+__device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
-// TMEM column of the 16-wide K slice kk of a 128-wide bf16 operand written by
-// the two compute halves: half 0 packs keys 0..63 into columns [0, 32), half 1
-// packs keys 64..127 into columns [64, 96) of the same region.
-__device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8; }
-
-// Store 64 values (this thread's half of a 128-wide row) as 32 packed bf16x2
-// columns starting at taddr.
-__device__ __forceinline__ void store_half_row_bf16(uint32_t taddr, const float (&v)[64]) {
-  uint32_t pk[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-  tmem_st16(taddr, pk);
-#pragma unroll
-  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(v[32 + 2 * e], v[32 + 2 * e + 1]);
-  tmem_st16(taddr + 16, pk);
-}
-
-__device__ __forceinline__ void load_half_row(uint32_t taddr, float (&v)[64]) {
+// Two 32-column TMEM loads of this thread's lane, waited for together.
+__device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float (&v0)[32], float (&v1)[32]) {
   uint32_t r0[32], r1[32];
-  tmem_ld32(taddr, r0);
-  tmem_ld32(taddr + 32, r1);
+  tmem_ld32(a0, r0);
+  tmem_ld32(a1, r1);
   tmem_ld_wait(r0);
   reg_tie(r1);
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
-    v[c] = __uint_as_float(r0[c]);
-    v[32 + c] = __uint_as_float(r1[c]);
+    v0[c] = __uint_as_float(r0[c]);
+    v1[c] = __uint_as_float(r1[c]);
   }
+}
+
+// 32 values as 16 packed bf16x2 columns at taddr.
+__device__ __forceinline__ void store_cols32_bf16(uint32_t taddr, const float (&v)[32]) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+  tmem_st16(taddr, pk);
 }
 
 // Write `ncols` fp32 TMEM columns of this thread's lane, times `mul`, as bf16
@@ -103,7 +106,8 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
     tmem_ld_wait(r);
     uint32_t pk[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+    for (int e = 0; e < 16; ++e)
+      pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
     if (valid) {
       uint4* d = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
@@ -112,40 +116,89 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
   }
 }
 
+// Shared-memory tiles: [rows][64] bf16 chunks, 128-byte swizzle; a tile of
+// head dimension D is D/64 chunks.  "Big" tiles have 128 rows, "small" 64.
 template <int D>
-struct BwdCfg {
+struct Tiles {
   static constexpr int kChunks = D / 64;
-  static constexpr int kChunkBytes = 128 * 64 * 2;
-  static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = 2;
-  // dK/dV kernel: K, V resident; Q and dO streamed.
-  // dQ kernel:    Q, dO resident; K and V streamed.
-  static constexpr int kOffA = 0;                          // resident tile 1
-  static constexpr int kOffB = kTileBytes;                 // resident tile 2
-  static constexpr int kOffX = 2 * kTileBytes;             // streamed tile 1, kStages deep
-  static constexpr int kOffY = kOffX + kStages * kTileBytes;  // streamed tile 2
-  static constexpr int kOffBar = kOffY + kStages * kTileBytes;
-  static constexpr int kOffRow = kOffBar + 512;            // per-stage LSE / Delta rows
-  static constexpr int kSmemBytes = kOffRow + 2 * 2 * 128 * 4 + 1024;
+  static constexpr int kBigChunk = 128 * kRowBytes;    // 16 KB
+  static constexpr int kSmallChunk = 64 * kRowBytes;   // 8 KB
+  static constexpr int kBigTile = kChunks * kBigChunk;
+  static constexpr int kSmallTile = kChunks * kSmallChunk;
+  // two resident big tiles, then kStages stages of two small tiles, then
+  // per-stage rows (LSE*log2e, Delta: 64 floats each), then barriers
+  static constexpr int kOffRes0 = 0;
+  static constexpr int kOffRes1 = kBigTile;
+  static constexpr int kOffX = 2 * kBigTile;
+  static constexpr int kOffY = kOffX + kStages * kSmallTile;
+  static constexpr int kOffRows = kOffY + kStages * kSmallTile;
+  static constexpr int kOffBar = kOffRows + kStages * 2 * 64 * 4;
+  static constexpr int kUsed = kOffBar + 512 + 1024;
+  // at least ~116 KB so that two CTAs never share an SM (each holds all 512
+  // TMEM columns)
+  static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmS = 0;     // S or S^T, 128 columns
-  static constexpr uint32_t kTmDP = 128;  // dP or dP^T, 128 columns
-  static constexpr uint32_t kTmAcc = 256; // dV then dK (dK/dV kernel) or dQ
+  static constexpr uint32_t kTmS = 0;      // S or S^T: 2 buffers x 64 columns
+  static constexpr uint32_t kTmDP = 128;   // dP or dP^T: 2 buffers x 64 columns
+  static constexpr uint32_t kTmAcc = 256;  // dV then dK (dK/dV kernel) or dQ
 };
 
 struct BwdBars {
-  uint64_t res_full;     // resident tiles loaded
-  uint64_t x_full[2];    // streamed stage loaded (both tiles)
-  uint64_t x_empty[2];   // streamed stage consumed by the MMAs
-  uint64_t s_full;       // S (S^T) in TMEM
-  uint64_t dp_full;      // dP (dP^T) in TMEM
-  uint64_t p_full;       // P^T written back (dK/dV kernel only)
-  uint64_t ds_full;      // dS (dS^T) written back
-  uint64_t acc_full;     // accumulators final
+  uint64_t res_full;
+  uint64_t x_full[kStages];
+  uint64_t x_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t dp_full[2];
+  uint64_t ds_full[2];  // P and dS of a buffer written back (256 compute threads)
+  uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+
+__device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) {
+  mbar_init(&bars->res_full, 1);
+  for (int i = 0; i < kStages; ++i) {
+    mbar_init(&bars->x_full[i], x_full_count);
+    mbar_init(&bars->x_empty[i], 1);
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&bars->s_full[i], 1);
+    mbar_init(&bars->dp_full[i], 1);
+    mbar_init(&bars->ds_full[i], kCompute);
+  }
+  mbar_init(&bars->acc_full, 1);
+  mbar_init(&bars->drain, 1);
+  bars->abort = 0;
+  fence_mbar_init();
+}
+
+// The D/16 MMAs of one [128 x N] product, A and B both K-major in shared
+// memory (A in a_chunk-byte chunks, B in b_chunk-byte chunks).  Descriptors
+// are built once and stepped by adding (bytes >> 4) to the start address.
+template <int D>
+__device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint32_t a_smem, int a_chunk, uint32_t b_smem, int b_chunk,
+                                         uint32_t idesc) {
+  const uint64_t a0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t b0 = sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t ao = (kk >> 2) * a_chunk + (kk & 3) * 32;
+    const uint32_t bo = (kk >> 2) * b_chunk + (kk & 3) * 32;
+    mma_ss(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// The 4 MMAs of acc (+)= A x B with A = 64 packed bf16 keys in TMEM and B =
+// [64 rows][D] in shared memory (MN-major, b_chunk-byte chunks).
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, int b_chunk,
+                                          uint32_t idesc, bool accumulate) {
+  const uint64_t b0 = sdesc_sw128(b_smem, b_chunk, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_ts(d_tmem, a_tmem + packed_slice_col(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+}
 
 // ============================================================== dK / dV
 
@@ -154,13 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                             const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = Tiles<D>;
+  constexpr int BQ = 64;   // query rows per streamed block
+  constexpr int BK = 128;  // key rows per CTA
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
-  float* srow = reinterpret_cast<float*>(smem + C::kOffRow);  // [2 buffers][LSE 128 | Delta 128]
+  float* srows = reinterpret_cast<float*>(smem + C::kOffRows);  // [stage][LSE*log2e 64 | Delta 64]
 
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
@@ -170,25 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int rep = s.H / s.HKV;
   int qlo, qhi;
-  q_range_for_kv(s.T, kBM, kBN, s.causal, s.window, kb, qlo, qhi);
+  q_range_for_kv(s.T, BQ, BK, s.causal, s.window, kb, qlo, qhi);
   const int nqb = qhi - qlo + 1;
   const int niter = rep * nqb;  // (head r, query block qb) pairs, r outer
 
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->res_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->x_full[i], 1);
-      mbar_init(&bars->x_empty[i], 1);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, kCompute);
-    mbar_init(&bars->ds_full, kCompute);
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_bars(bars, 1 + 32);
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
@@ -207,69 +247,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kBigTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmK, &bars->res_full, smem + C::kOffA + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
-        tma_load_3d(&tmV, &bars->res_full, smem + C::kOffB + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+        tma_load_3d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kBigChunk, g * D + c * 64, kb * BK, b);
+        tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kBigChunk, g * D + c * 64, kb * BK, b);
       }
-      int issued = 0;
-      for (int n = 0; n < niter; ++n) {
-        const int st = n & 1;
-        if (n >= 2 && !wait_bar(&bars->x_empty[st], ((n >> 1) - 1) & 1, ctl, kCode)) break;
-        const int h = g * rep + n / nqb;
-        const int qb = qlo + n % nqb;
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTileBytes);
+    }
+    int issued = 0;
+    for (int n = 0; n < niter; ++n) {
+      const int st = n % kStages;
+      if (n >= kStages && !warp_wait(&bars->x_empty[st], ((n / kStages) - 1) & 1, ctl, kCode)) break;
+      const int h = g * rep + n / nqb;
+      const int qb = qlo + n % nqb;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kSmallTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTileBytes + c * C::kChunkBytes,
-                      h * D + c * 64, qb * kBM, b);
-          tma_load_3d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTileBytes + c * C::kChunkBytes,
-                      h * D + c * 64, qb * kBM, b);
+          tma_load_3d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kSmallTile + c * C::kSmallChunk,
+                      h * D + c * 64, qb * BQ, b);
+          tma_load_3d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kSmallTile + c * C::kSmallChunk,
+                      h * D + c * 64, qb * BQ, b);
         }
-        issued = n + 1;
       }
-      if (bars->abort) {
-        drain_bar(&bars->res_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued - 2); n < issued; ++n) drain_bar(&bars->x_full[n & 1], (n >> 1) & 1, p.timeout_ns);
+      // LSE (pre-scaled to base 2) and Delta of the block's 64 query rows
+      float* rows = srows + st * 128;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = lane + 32 * k;
+        const int i = qb * BQ + r;
+        float l2 = 0.f, dl = 0.f;
+        if (i < s.T) {
+          const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
+          l2 = p.LSE[idx] * kLog2e;
+          dl = p.Delta[idx];
+        }
+        rows[r] = l2;
+        rows[64 + r] = dl;
       }
+      mbar_arrive(&bars->x_full[st]);
+      issued = n + 1;
+    }
+    if (lane == 0 && bars->abort) {
+      drain_bar(&bars->res_full, 0, p.timeout_ns);
+      for (int n = imax(0, issued - kStages); n < issued; ++n)
+        drain_bar(&bars->x_full[n % kStages], (n / kStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // K-major x K-major
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);   // TMEM A x MN-major B
-      const uint32_t sK = sbase + C::kOffA;
-      const uint32_t sV = sbase + C::kOffB;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BQ, false, false);  // K-major x K-major, N = 64
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
+      const uint32_t sK = sbase + C::kOffRes0;
+      const uint32_t sV = sbase + C::kOffRes1;
+      // S^T_n = K Q_n^T and dP^T_n = V dO_n^T into buffer n & 1
+      auto issue_sdp = [&](int n) -> bool {
+        const int st = n % kStages;
+        const int bf = n & 1;
+        if (!wait_bar(&bars->x_full[st], (n / kStages) & 1, ctl, kCode)) return false;
+        tc_fence_after();
+        issue_kk<D>(tmem + C::kTmS + bf * 64, sK, C::kBigChunk, sbase + C::kOffX + st * C::kSmallTile,
+                    C::kSmallChunk, idesc_s);
+        mma_commit(&bars->s_full[bf]);
+        issue_kk<D>(tmem + C::kTmDP + bf * 64, sV, C::kBigChunk, sbase + C::kOffY + st * C::kSmallTile,
+                    C::kSmallChunk, idesc_s);
+        mma_commit(&bars->dp_full[bf]);
+        return true;
+      };
       bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
+      if (ok && niter > 0) ok = issue_sdp(0);
       for (int n = 0; ok && n < niter; ++n) {
-        const int st = n & 1;
-        const uint32_t sQ = sbase + C::kOffX + st * C::kTileBytes;
-        const uint32_t sdO = sbase + C::kOffY + st * C::kTileBytes;
-        if (!(ok = wait_bar(&bars->x_full[st], (n >> 1) & 1, ctl, kCode))) break;
+        if (n + 1 < niter && !(ok = issue_sdp(n + 1))) break;
+        const int st = n % kStages;
+        const int bf = n & 1;
+        if (!(ok = wait_bar(&bars->ds_full[bf], (n >> 1) & 1, ctl, kCode))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K Q^T
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&bars->s_full);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO + off, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&bars->dp_full);
-        if (!(ok = wait_bar(&bars->p_full, n & 1, ctl, kCode))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)  // dV += P^T dO   (K = query rows)
-          mma_ts(tmem + C::kTmAcc, tmem + C::kTmS + packed_slice_col(kk),
-                 sdesc_sw128(sdO + kk * 2048, C::kChunkBytes, 1024), idesc_acc, (n > 0 || kk > 0));
-        if (!(ok = wait_bar(&bars->ds_full, n & 1, ctl, kCode))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)  // dK += dS^T Q
-          mma_ts(tmem + C::kTmAcc + D, tmem + C::kTmDP + packed_slice_col(kk),
-                 sdesc_sw128(sQ + kk * 2048, C::kChunkBytes, 1024), idesc_acc, (n > 0 || kk > 0));
+        // dV += P^T dO ; dK += dS^T Q   (K = the block's 64 query rows)
+        issue_acc(tmem + C::kTmAcc, tmem + C::kTmS + bf * 64, sbase + C::kOffY + st * C::kSmallTile,
+                  C::kSmallChunk, idesc_acc, n > 0);
+        issue_acc(tmem + C::kTmAcc + D, tmem + C::kTmDP + bf * 64, sbase + C::kOffX + st * C::kSmallTile,
+                  C::kSmallChunk, idesc_acc, n > 0);
         mma_commit(&bars->x_empty[st]);
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -278,54 +333,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- compute
-    const int tid = threadIdx.x;        // 0..255
-    const int quarter = warp & 3;       // TMEM lane quarter
-    const int half = warp >> 2;         // column half
-    const int jrow = quarter * 32 + lane;  // KV row within the block (TMEM lane)
-    const int j = kb * kBN + jrow;
+    const int quarter = warp & 3;          // TMEM lane quarter
+    const int half = warp >> 2;            // 32-column half of each tile
+    const int jrow = quarter * 32 + lane;  // key row within the block (TMEM lane)
+    const int j = kb * BK + jrow;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int n = 0; n < niter; ++n) {
-      const int h = g * rep + n / nqb;
+    for (int n = 0; ok && n < niter; ++n) {
+      const int st = n % kStages;
+      const int bf = n & 1;
       const int qb = qlo + n % nqb;
-      // stage LSE*log2e and Delta of the 128 query rows into shared memory
-      float* buf = srow + (n & 1) * 256;
-      {
-        const int r = tid & 127;
-        const int i = qb * kBM + r;
-        const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
-        float v = 0.f;
-        if (i < s.T) v = (tid < 128) ? p.LSE[idx] * kLog2e : p.Delta[idx];
-        buf[tid] = v;
-      }
-      compute_sync();
-      if (!(ok = warp_wait(&bars->s_full, n & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->dp_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->x_full[st], (n / kStages) & 1, ctl, kCode))) break;  // rows visible
       tc_fence_after();
-      float pv[64];
-      load_half_row(tmem + lane_addr + C::kTmS + half * 64, pv);
-      const bool need_mask = block_needs_mask(s.T, kBM, kBN, s.causal, s.window, qb, kb);
+      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 64 + half * 32;
+      const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + bf * 64 + half * 32;
+      float pv[32], ds[32];
+      load_two_cols32(s_addr, dp_addr, pv, ds);
+      const float4* lse4 = reinterpret_cast<const float4*>(srows + st * 128 + half * 32);
+      const float4* del4 = reinterpret_cast<const float4*>(srows + st * 128 + 64 + half * 32);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int ic = half * 64 + c;  // query row within the block
-        float e = ex2(fmaf(pv[c], sl2, -buf[ic]));
-        if (need_mask && masked(s.T, s.causal, s.window, qb * kBM + ic, j)) e = 0.f;
-        pv[c] = e;
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 l = lse4[c4];
+        const float4 d = del4[c4];
+        pv[4 * c4 + 0] = ex2(fmaf(pv[4 * c4 + 0], sl2, -l.x));
+        pv[4 * c4 + 1] = ex2(fmaf(pv[4 * c4 + 1], sl2, -l.y));
+        pv[4 * c4 + 2] = ex2(fmaf(pv[4 * c4 + 2], sl2, -l.z));
+        pv[4 * c4 + 3] = ex2(fmaf(pv[4 * c4 + 3], sl2, -l.w));
+        ds[4 * c4 + 0] -= d.x;
+        ds[4 * c4 + 1] -= d.y;
+        ds[4 * c4 + 2] -= d.z;
+        ds[4 * c4 + 3] -= d.w;
       }
-      store_half_row_bf16(tmem + lane_addr + C::kTmS + half * 64, pv);
+      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
+        const int i0 = qb * BQ + half * 32;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
+      }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) ds[c] *= pv[c];  // dS^T = P^T (dP^T - Delta)
+      store_cols32_bf16(s_addr, pv);
+      store_cols32_bf16(dp_addr, ds);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full);
-      if (!(ok = warp_wait(&bars->dp_full, n & 1, ctl, kCode))) break;
-      tc_fence_after();
-      float dp[64];
-      load_half_row(tmem + lane_addr + C::kTmDP + half * 64, dp);
-#pragma unroll
-      for (int c = 0; c < 64; ++c) dp[c] = pv[c] * (dp[c] - buf[128 + half * 64 + c]);
-      store_half_row_bf16(tmem + lane_addr + C::kTmDP + half * 64, dp);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive(&bars->ds_full[bf]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
@@ -333,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D + half * (D / 2);
       store_acc_row(tmem + lane_addr + C::kTmAcc + half * (D / 2), D / 2, 1.f,
                     static_cast<__nv_bfloat16*>(p.dV) + rowoff, j < s.T);
-      store_acc_row(tmem + lane_addr + C::kTmAcc + D + half * (D / 2), D / 2, p.s.scale,
+      store_acc_row(tmem + lane_addr + C::kTmAcc + D + half * (D / 2), D / 2, s.scale,
                     static_cast<__nv_bfloat16*>(p.dK) + rowoff, j < s.T);
     }
   }
@@ -354,40 +407,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                           const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = Tiles<D>;
+  constexpr int BQ = 128;  // query rows per CTA
+  constexpr int BK = 64;   // key rows per streamed block
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
 
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nq = ceil_div(s.T, kBM);
+  const int nq = ceil_div(s.T, BQ);
   const int qb = nq - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int g = h / (s.H / s.HKV);
   int kb_lo, kb_hi;
-  kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, qb, kb_lo, kb_hi);
+  kv_range_for_q(s.T, BQ, BK, s.causal, s.window, qb, kb_lo, kb_hi);
   const int nblk = kb_hi - kb_lo + 1;
 
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->res_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->x_full[i], 1);
-      mbar_init(&bars->x_empty[i], 1);
-    }
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->p_full, kCompute);
-    mbar_init(&bars->ds_full, kCompute);
-    mbar_init(&bars->acc_full, 1);
-    mbar_init(&bars->drain, 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_bars(bars, 1);
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
@@ -405,61 +445,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kBigTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmQ, &bars->res_full, smem + C::kOffA + c * C::kChunkBytes, h * D + c * 64, qb * kBM, b);
-        tma_load_3d(&tmdO, &bars->res_full, smem + C::kOffB + c * C::kChunkBytes, h * D + c * 64, qb * kBM, b);
+        tma_load_3d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kBigChunk, h * D + c * 64, qb * BQ, b);
+        tma_load_3d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kBigChunk, h * D + c * 64, qb * BQ, b);
       }
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
-        const int st = n & 1;
-        if (n >= 2 && !wait_bar(&bars->x_empty[st], ((n >> 1) - 1) & 1, ctl, kCode)) break;
+        const int st = n % kStages;
+        if (n >= kStages && !wait_bar(&bars->x_empty[st], ((n / kStages) - 1) & 1, ctl, kCode)) break;
         const int kb = kb_lo + n;
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kSmallTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffX + st * C::kTileBytes + c * C::kChunkBytes,
-                      g * D + c * 64, kb * kBN, b);
-          tma_load_3d(&tmV, &bars->x_full[st], smem + C::kOffY + st * C::kTileBytes + c * C::kChunkBytes,
-                      g * D + c * 64, kb * kBN, b);
+          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffX + st * C::kSmallTile + c * C::kSmallChunk,
+                      g * D + c * 64, kb * BK, b);
+          tma_load_3d(&tmV, &bars->x_full[st], smem + C::kOffY + st * C::kSmallTile + c * C::kSmallChunk,
+                      g * D + c * 64, kb * BK, b);
         }
         issued = n + 1;
       }
       if (bars->abort) {
         drain_bar(&bars->res_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued - 2); n < issued; ++n) drain_bar(&bars->x_full[n & 1], (n >> 1) & 1, p.timeout_ns);
+        for (int n = imax(0, issued - kStages); n < issued; ++n)
+          drain_bar(&bars->x_full[n % kStages], (n / kStages) & 1, p.timeout_ns);
       }
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);
-      const uint32_t sQ = sbase + C::kOffA;
-      const uint32_t sdO = sbase + C::kOffB;
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false, false);  // K-major x K-major, N = 64
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
+      const uint32_t sQ = sbase + C::kOffRes0;
+      const uint32_t sdO = sbase + C::kOffRes1;
+      // S_n = Q K_n^T and dP_n = dO V_n^T into buffer n & 1
+      auto issue_sdp = [&](int n) -> bool {
+        const int st = n % kStages;
+        const int bf = n & 1;
+        if (!wait_bar(&bars->x_full[st], (n / kStages) & 1, ctl, kCode)) return false;
+        tc_fence_after();
+        issue_kk<D>(tmem + C::kTmS + bf * 64, sQ, C::kBigChunk, sbase + C::kOffX + st * C::kSmallTile,
+                    C::kSmallChunk, idesc_s);
+        mma_commit(&bars->s_full[bf]);
+        issue_kk<D>(tmem + C::kTmDP + bf * 64, sdO, C::kBigChunk, sbase + C::kOffY + st * C::kSmallTile,
+                    C::kSmallChunk, idesc_s);
+        mma_commit(&bars->dp_full[bf]);
+        return true;
+      };
       bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
+      if (ok && nblk > 0) ok = issue_sdp(0);
       for (int n = 0; ok && n < nblk; ++n) {
-        const int st = n & 1;
-        const uint32_t sK = sbase + C::kOffX + st * C::kTileBytes;
-        const uint32_t sV = sbase + C::kOffY + st * C::kTileBytes;
-        if (!(ok = wait_bar(&bars->x_full[st], (n >> 1) & 1, ctl, kCode))) break;
+        if (n + 1 < nblk && !(ok = issue_sdp(n + 1))) break;
+        const int st = n % kStages;
+        const int bf = n & 1;
+        if (!(ok = wait_bar(&bars->ds_full[bf], (n >> 1) & 1, ctl, kCode))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S = Q K^T
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&bars->s_full);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP = dO V^T
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kTmDP, sdesc_sw128(sdO + off, 16, 1024), sdesc_sw128(sV + off, 16, 1024), idesc_s, kk > 0);
-        }
-        mma_commit(&bars->dp_full);
-        if (!(ok = wait_bar(&bars->ds_full, n & 1, ctl, kCode))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)  // dQ += dS K   (K = key rows)
-          mma_ts(tmem + C::kTmAcc, tmem + C::kTmS + packed_slice_col(kk),
-                 sdesc_sw128(sK + kk * 2048, C::kChunkBytes, 1024), idesc_acc, (n > 0 || kk > 0));
+        // dQ += dS K   (K = the block's 64 key rows)
+        issue_acc(tmem + C::kTmAcc, tmem + C::kTmS + bf * 64, sbase + C::kOffX + st * C::kSmallTile,
+                  C::kSmallChunk, idesc_acc, n > 0);
         mma_commit(&bars->x_empty[st]);
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -470,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = warp >> 2;
     const int irow = quarter * 32 + lane;
-    const int i = qb * kBM + irow;
+    const int i = qb * BQ + irow;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     float lse2 = 0.f, delta = 0.f;
@@ -480,35 +521,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       delta = p.Delta[idx];
     }
     bool ok = true;
-    for (int n = 0; n < nblk; ++n) {
+    for (int n = 0; ok && n < nblk; ++n) {
       const int kb = kb_lo + n;
-      if (!(ok = warp_wait(&bars->s_full, n & 1, ctl, kCode))) break;
+      const int bf = n & 1;
+      if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->dp_full[bf], (n >> 1) & 1, ctl, kCode))) break;
       tc_fence_after();
-      float pv[64];
-      load_half_row(tmem + lane_addr + C::kTmS + half * 64, pv);
-      const bool need_mask = block_needs_mask(s.T, kBM, kBN, s.causal, s.window, qb, kb);
+      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 64 + half * 32;
+      float pv[32], ds[32];
+      load_two_cols32(s_addr, tmem + lane_addr + C::kTmDP + bf * 64 + half * 32, pv, ds);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float e = ex2(fmaf(pv[c], sl2, -lse2));
-        if (need_mask && masked(s.T, s.causal, s.window, i, kb * kBN + half * 64 + c)) e = 0.f;
-        pv[c] = e;
+      for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], sl2, -lse2));
+      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
+        const int j0 = kb * BK + half * 32;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
       }
-      if (!(ok = warp_wait(&bars->dp_full, n & 1, ctl, kCode))) break;
-      tc_fence_after();
-      float dp[64];
-      load_half_row(tmem + lane_addr + C::kTmDP + half * 64, dp);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) dp[c] = pv[c] * (dp[c] - delta);
-      store_half_row_bf16(tmem + lane_addr + C::kTmS + half * 64, dp);
+      for (int c = 0; c < 32; ++c) ds[c] = pv[c] * (ds[c] - delta);  // dS = P (dP - Delta)
+      store_cols32_bf16(s_addr, ds);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full);
+      mbar_arrive(&bars->ds_full[bf]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * D + half * (D / 2);
-      store_acc_row(tmem + lane_addr + C::kTmAcc + half * (D / 2), D / 2, p.s.scale,
+      store_acc_row(tmem + lane_addr + C::kTmAcc + half * (D / 2), D / 2, s.scale,
                     static_cast<__nv_bfloat16*>(p.dQ) + rowoff, i < s.T);
     }
   }
@@ -524,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = Tiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -532,14 +572,14 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(p.s.T, kBN), p.s.HKV, p.s.B);
-  fa_bwd_dkdv_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
+  dim3 grid(ceil_div(p.s.T, 128), p.s.HKV, p.s.B);
+  fa_bwd_dkdv_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q64, tm.k, tm.v, tm.dO64, p);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  using C = BwdCfg<D>;
+  using C = Tiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -547,8 +587,8 @@ cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t s
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(p.s.T, kBM), p.s.H, p.s.B);
-  fa_bwd_dq_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
+  dim3 grid(ceil_div(p.s.T, 128), p.s.H, p.s.B);
+  fa_bwd_dq_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k64, tm.v64, tm.dO, p);
   return cudaGetLastError();
 }
 

@@ -44,8 +44,9 @@ struct FwdCfg {
   static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmS = 0;      // S[0] at 0, S[1] at 128
-  static constexpr uint32_t kTmO = 256;    // O: D columns
+  static constexpr uint32_t kTmQ = 0;      // Q as bf16 A operand: D/2 columns
+  static constexpr uint32_t kTmS = 128;    // S[0] at 128, S[1] at 256
+  static constexpr uint32_t kTmO = 384;    // O: D columns
 };
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P <= 256 between rescales
@@ -53,6 +54,7 @@ constexpr int kThreads = 192;
 
 struct Bars {
   uint64_t q_full;
+  uint64_t q_tmem;  // Q copied into TMEM by the 128 softmax threads
   uint64_t k_full[4];
   uint64_t v_full[4];
   uint64_t kv_empty[4];
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_tmem, 128);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
@@ -171,8 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-      const uint32_t sq = sbase + C::kOffQ;
-      bool ok = wait_bar(&bars->q_full, 0, ctl, kCode);
+      bool ok = wait_bar(&bars->q_tmem, 0, ctl, kCode);
       for (int n = 0; ok && n <= nblk; ++n) {
         if (n < nblk) {
           const int st = n % C::kStages;
@@ -183,8 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kTmS + sb * 128, sdesc_sw128(sq + off, 16, 1024), sdesc_sw128(sk + off, 16, 1024),
-                   idesc_s, kk > 0);
+            mma_ts(tmem + C::kTmS + sb * 128, tmem + C::kTmQ + kk * 8, sdesc_sw128(sk + off, 16, 1024), idesc_s,
+                   kk > 0);
           }
           mma_commit(&bars->s_full[sb]);
         }
@@ -218,8 +220,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     float m_run = -CUDART_INF_F;  // reference max, log2 domain
     float l_run = 0.f;
-    bool ok = true;
-    for (int n = 0; n < nblk; ++n) {
+    // Q into TMEM (row t on lane t) as the A operand of every S MMA, so that
+    // those MMAs read only K from shared memory
+    bool ok = warp_wait(&bars->q_full, 0, ctl, kCode);
+    if (ok) {
+      tile_row_to_tmem<D>(smem + C::kOffQ, C::kChunkBytes, t, tmem + lane_addr + C::kTmQ);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->q_tmem);
+    }
+    for (int n = 0; ok && n < nblk; ++n) {
       const int kb = kb_lo + n;
       const int sb = n & 1;
       if (!(ok = warp_wait(&bars->s_full[sb], (n >> 1) & 1, ctl, kCode))) break;

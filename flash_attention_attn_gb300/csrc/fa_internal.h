@@ -88,8 +88,11 @@ struct BwdParams {
   uint64_t timeout_ns;
 };
 
+// 3-D views [B][T][heads*D] with boxes of 64 elements x R rows x 1 batch:
+// R = 128 for the plain maps, R = 64 for the *64 maps.
 struct TensorMaps {
-  CUtensorMap q, k, v, o, dO;  // 3-D views [B][T][heads*D], box 64 x 128 x 1
+  CUtensorMap q, k, v, dO;
+  CUtensorMap q64, k64, v64, dO64;
 };
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);

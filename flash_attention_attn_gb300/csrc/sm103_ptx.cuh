@@ -258,6 +258,28 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Copy row `row` of a swizzled [128][D] bf16 tile (D/64 chunks of
+// chunk_bytes) from shared memory into TMEM columns [taddr, taddr + D/2) of
+// this thread's lane, two bf16 per column: the layout of an MMA A operand.
+// 128-byte swizzle: logical 16-byte unit u of row r sits at unit u ^ (r & 7).
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int chunk_bytes, int row, uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    const uint8_t* rp = tile + c * chunk_bytes + row * 128;
+    uint32_t r[32];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint4 v = *reinterpret_cast<const uint4*>(rp + ((u ^ (row & 7)) << 4));
+      r[4 * u + 0] = v.x;
+      r[4 * u + 1] = v.y;
+      r[4 * u + 2] = v.z;
+      r[4 * u + 3] = v.w;
+    }
+    tmem_st32(taddr + c * 32, r);
+  }
+}
+
 // ------------------------------------------------------------------ math
 
 // 2^x on the special-function unit (ex2.approx, flush-to-zero).
