@@ -402,14 +402,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ================================================================== dQ
 
+// dQ tiles: 128-row query tile (Q, dO resident), 128-row K/V blocks streamed,
+// so every score MMA is [128 x 128 x 16] (a 64-wide one runs at 2/3 rate).
+// TMEM: S double-buffered (2 x 128 columns), dP single (128), dQ (D).  dP of
+// block n+1 is computed as soon as the compute warps have released block n.
+template <int D>
+struct DqTiles {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunk = 128 * kRowBytes;  // [128][64] bf16 = 16 KB
+  static constexpr int kTile = kChunks * kChunk;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kOffRes0 = 0;               // Q
+  static constexpr int kOffRes1 = kTile;           // dO
+  static constexpr int kOffX = 2 * kTile;          // K stages
+  static constexpr int kOffY = kOffX + kStages * kTile;  // V stages
+  static constexpr int kOffBar = kOffY + kStages * kTile;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmS = 0;     // 2 x 128 columns
+  static constexpr uint32_t kTmDP = 256;  // 128 columns
+  static constexpr uint32_t kTmDQ = 384;  // D columns
+};
+
+// TMEM column of 16-key slice kk (0..7) of a 128-key bf16 dS row that the two
+// compute halves packed: half h writes keys [64h, 64h + 64) into columns
+// [64h, 64h + 32).
+__device__ __forceinline__ uint32_t packed_slice_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                           const BwdParams p) {
-  using C = Tiles<D>;
+  using C = DqTiles<D>;
   constexpr int BQ = 128;  // query rows per CTA
-  constexpr int BK = 64;   // key rows per streamed block
+  constexpr int BK = 128;  // key rows per streamed block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -445,62 +472,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kBigTile);
+      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kBigChunk, h * D + c * 64, qb * BQ, b);
-        tma_load_3d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kBigChunk, h * D + c * 64, qb * BQ, b);
+        tma_load_3d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, h * D + c * 64, qb * BQ, b);
+        tma_load_3d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, h * D + c * 64, qb * BQ, b);
       }
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
-        const int st = n % kStages;
-        if (n >= kStages && !wait_bar(&bars->x_empty[st], ((n / kStages) - 1) & 1, ctl, kCode)) break;
+        const int st = n % C::kStages;
+        if (n >= C::kStages && !wait_bar(&bars->x_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
         const int kb = kb_lo + n;
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kSmallTile);
+        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffX + st * C::kSmallTile + c * C::kSmallChunk,
-                      g * D + c * 64, kb * BK, b);
-          tma_load_3d(&tmV, &bars->x_full[st], smem + C::kOffY + st * C::kSmallTile + c * C::kSmallChunk,
-                      g * D + c * 64, kb * BK, b);
+          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, g * D + c * 64,
+                      kb * BK, b);
+          tma_load_3d(&tmV, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, g * D + c * 64,
+                      kb * BK, b);
         }
         issued = n + 1;
       }
       if (bars->abort) {
         drain_bar(&bars->res_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued - kStages); n < issued; ++n)
-          drain_bar(&bars->x_full[n % kStages], (n / kStages) & 1, p.timeout_ns);
+        for (int n = imax(0, issued - C::kStages); n < issued; ++n)
+          drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
       }
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false, false);  // K-major x K-major, N = 64
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false, false);  // K-major x K-major, N = 128
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sQ = sbase + C::kOffRes0;
       const uint32_t sdO = sbase + C::kOffRes1;
-      // S_n = Q K_n^T and dP_n = dO V_n^T into buffer n & 1
-      auto issue_sdp = [&](int n) -> bool {
-        const int st = n % kStages;
-        const int bf = n & 1;
-        if (!wait_bar(&bars->x_full[st], (n / kStages) & 1, ctl, kCode)) return false;
+      auto issue_s = [&](int n) -> bool {  // S_n = Q K_n^T into buffer n & 1
+        const int st = n % C::kStages;
+        if (!wait_bar(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
-        issue_kk<D>(tmem + C::kTmS + bf * 64, sQ, C::kBigChunk, sbase + C::kOffX + st * C::kSmallTile,
-                    C::kSmallChunk, idesc_s);
-        mma_commit(&bars->s_full[bf]);
-        issue_kk<D>(tmem + C::kTmDP + bf * 64, sdO, C::kBigChunk, sbase + C::kOffY + st * C::kSmallTile,
-                    C::kSmallChunk, idesc_s);
-        mma_commit(&bars->dp_full[bf]);
+        issue_kk<D>(tmem + C::kTmS + (n & 1) * 128, sQ, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk,
+                    idesc_s);
+        mma_commit(&bars->s_full[n & 1]);
         return true;
       };
+      auto issue_dp = [&](int n) {  // dP_n = dO V_n^T (its stage was waited for by issue_s)
+        issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffY + (n % C::kStages) * C::kTile, C::kChunk,
+                    idesc_s);
+        mma_commit(&bars->dp_full[0]);
+      };
       bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
-      if (ok && nblk > 0) ok = issue_sdp(0);
+      if (ok && nblk > 0) {
+        ok = issue_s(0);
+        if (ok) issue_dp(0);
+      }
+      // queue order: S0 dP0 S1 | dP1 dQ0 S2 | dP2 dQ1 S3 ...
       for (int n = 0; ok && n < nblk; ++n) {
-        if (n + 1 < nblk && !(ok = issue_sdp(n + 1))) break;
-        const int st = n % kStages;
-        const int bf = n & 1;
-        if (!(ok = wait_bar(&bars->ds_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+        if (n + 1 < nblk && !(ok = issue_s(n + 1))) break;
+        const int st = n % C::kStages;
+        if (!(ok = wait_bar(&bars->ds_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
-        // dQ += dS K   (K = the block's 64 key rows)
-        issue_acc(tmem + C::kTmAcc, tmem + C::kTmS + bf * 64, sbase + C::kOffX + st * C::kSmallTile,
-                  C::kSmallChunk, idesc_acc, n > 0);
+        if (n + 1 < nblk) issue_dp(n + 1);  // dP_n has been read: its columns are free
+        // dQ += dS K   (K = the block's 128 key rows)
+        const uint64_t b0 = sdesc_sw128(sbase + C::kOffX + st * C::kTile, C::kChunk, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ts(tmem + C::kTmDQ, tmem + C::kTmS + (n & 1) * 128 + packed_slice_col128(kk),
+                 b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&bars->x_empty[st]);
       }
       if (ok) mma_commit(&bars->acc_full);
@@ -509,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int quarter = warp & 3;
-    const int half = warp >> 2;
+    const int half = warp >> 2;  // 64-key half of each 128-key block
     const int irow = quarter * 32 + lane;
     const int i = qb * BQ + irow;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -525,30 +559,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kb = kb_lo + n;
       const int bf = n & 1;
       if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
-      if (!(ok = warp_wait(&bars->dp_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 64 + half * 32;
-      float pv[32], ds[32];
-      load_two_cols32(s_addr, tmem + lane_addr + C::kTmDP + bf * 64 + half * 32, pv, ds);
+      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 128 + half * 64;
+      const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
+      const bool need_mask = block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], sl2, -lse2));
-      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
-        const int j0 = kb * BK + half * 32;
+      for (int part = 0; part < 2; ++part) {  // 32 keys at a time
+        float pv[32], ds[32];
+        load_two_cols32(s_addr + part * 32, dp_addr + part * 32, pv, ds);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+        for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], sl2, -lse2));
+        if (need_mask) {
+          const int j0 = kb * BK + half * 64 + part * 32;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) ds[c] = pv[c] * (ds[c] - delta);  // dS = P (dP - Delta)
+        // packed dS of keys [32 part, 32 part + 32) into columns [16 part, 16 part + 16)
+        // of this half's region (already read)
+        store_cols32_bf16(s_addr + part * 16, ds);
       }
-#pragma unroll
-      for (int c = 0; c < 32; ++c) ds[c] = pv[c] * (ds[c] - delta);  // dS = P (dP - Delta)
-      store_cols32_bf16(s_addr, ds);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full[bf]);
+      mbar_arrive(&bars->ds_full[0]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * D + half * (D / 2);
-      store_acc_row(tmem + lane_addr + C::kTmAcc + half * (D / 2), D / 2, s.scale,
+      store_acc_row(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.scale,
                     static_cast<__nv_bfloat16*>(p.dQ) + rowoff, i < s.T);
     }
   }
@@ -579,7 +620,7 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
 
 template <int D>
 cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  using C = Tiles<D>;
+  using C = DqTiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -588,7 +629,7 @@ cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t s
     attr_set = true;
   }
   dim3 grid(ceil_div(p.s.T, 128), p.s.H, p.s.B);
-  fa_bwd_dq_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k64, tm.v64, tm.dO, p);
+  fa_bwd_dq_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }
 
