@@ -4,7 +4,7 @@
 //
 // dK/dV: one CTA per (b, kv head g, 128-row KV block).  K and V stay in
 //   shared memory and dK, dV in TMEM for the CTA's whole life while it visits
-//   every query head of the group and every 64-row query block that sees the
+//   every query head of the group and every 128-row query block that sees the
 //   KV block.  Accumulation is private to the CTA: no atomics.
 //     S^T  = K Q^T          (TMEM, KV rows on lanes)
 //     dP^T = V dO^T
@@ -16,24 +16,24 @@
 //   the group's query heads; teeny-kernels flash_attn2.rs,
 //   flash_attention2_backward_dkv: no atomics are needed.)
 //
-// dQ: one CTA per (b, h, 128-row query block); loops over the visible 64-row
+// dQ: one CTA per (b, h, 128-row query block); loops over the visible 128-row
 //   KV blocks in a fixed order, so the result is bitwise reproducible.
 //     S = Q K^T ; dP = dO V^T ; dS = P (dP - Delta) -> bf16, TMEM ; dQ += dS K
 //   and at the end dQ *= scale.  (forge flash_attention.metal,
 //   flash_attn_bwd_dq; teeny-kernels flash_attention2_backward_dq.)
 //
-// Pipelining: the score and dP tiles are 64 columns wide and double-buffered
-// in TMEM, so the MMA warp computes block n+1's S and dP while the compute
-// warps work on block n.  The compute warps load S and dP of a block
-// together, produce P and dS in one pass, store them and signal once; the
-// MMA warp then queues the accumulator MMAs of the block.  The per-row LSE
-// and Delta of each streamed query block travel with its stage (the
-// producer warp loads them next to the TMA copies).
+// Both kernels use 128 x 128 score tiles, so every MMA is [128 x 128 x 16] or
+// wider: a tcgen05 MMA with N = 64 was measured on GB300 at 48 cycles
+// against 64 for N = 128 (2/3 of the rate).  TMEM holds the fp32 score and
+// dP tiles, the bf16 P and dS written back over them (the A operands of the
+// accumulator MMAs) and the accumulators.  The per-row LSE and Delta of each
+// streamed query block travel with its shared-memory stage (the producer
+// warp loads them next to the TMA copies).
 //
 // Warp roles in both kernels: warps 0-7 compute (warp w owns TMEM lanes
-// 32*(w%4).. and the 32-column half w/4 of each 64-column tile), warp 8 TMA
+// 32*(w%4).. and the 64-column half w/4 of each 128-column tile), warp 8 TMA
 // producer, warp 9 MMA issuer and TMEM owner.  Each half writes its bf16
-// results back into the first 16 columns of the 32 it read, so no half
+// results back into the first 32 columns of the 64 it read, so no half
 // overwrites data the other still has to load.
 #include <cuda_bf16.h>
 #include <math_constants.h>
@@ -68,11 +68,6 @@ __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
                  "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
-
-// TMEM column of the 16-wide K slice kk (0..3) of a 64-wide bf16 operand that
-// the two compute halves wrote: half 0 packs elements 0..31 into columns
-// [0, 16), half 1 packs elements 32..63 into columns [32, 48).
-__device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 // Two 32-column TMEM loads of this thread's lane, waited for together.
 __device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float (&v0)[32], float (&v1)[32]) {
@@ -116,40 +111,14 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
   }
 }
 
-// Shared-memory tiles: [rows][64] bf16 chunks, 128-byte swizzle; a tile of
-// head dimension D is D/64 chunks.  "Big" tiles have 128 rows, "small" 64.
-template <int D>
-struct Tiles {
-  static constexpr int kChunks = D / 64;
-  static constexpr int kBigChunk = 128 * kRowBytes;    // 16 KB
-  static constexpr int kSmallChunk = 64 * kRowBytes;   // 8 KB
-  static constexpr int kBigTile = kChunks * kBigChunk;
-  static constexpr int kSmallTile = kChunks * kSmallChunk;
-  // two resident big tiles, then kStages stages of two small tiles, then
-  // per-stage rows (LSE*log2e, Delta: 64 floats each), then barriers
-  static constexpr int kOffRes0 = 0;
-  static constexpr int kOffRes1 = kBigTile;
-  static constexpr int kOffX = 2 * kBigTile;
-  static constexpr int kOffY = kOffX + kStages * kSmallTile;
-  static constexpr int kOffRows = kOffY + kStages * kSmallTile;
-  static constexpr int kOffBar = kOffRows + kStages * 2 * 64 * 4;
-  static constexpr int kUsed = kOffBar + 512 + 1024;
-  // at least ~116 KB so that two CTAs never share an SM (each holds all 512
-  // TMEM columns)
-  static constexpr int kSmemBytes = kUsed > 120 * 1024 ? kUsed : 120 * 1024;
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmS = 0;      // S or S^T: 2 buffers x 64 columns
-  static constexpr uint32_t kTmDP = 128;   // dP or dP^T: 2 buffers x 64 columns
-  static constexpr uint32_t kTmAcc = 256;  // dV then dK (dK/dV kernel) or dQ
-};
-
 struct BwdBars {
   uint64_t res_full;
   uint64_t x_full[kStages];
   uint64_t x_empty[kStages];
   uint64_t s_full[2];
   uint64_t dp_full[2];
-  uint64_t ds_full[2];  // P and dS of a buffer written back (256 compute threads)
+  uint64_t p_full[2];   // P written back (256 compute threads)
+  uint64_t ds_full[2];  // dS (and P) written back (256 compute threads)
   uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
@@ -165,6 +134,7 @@ __device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) 
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bars->s_full[i], 1);
     mbar_init(&bars->dp_full[i], 1);
+    mbar_init(&bars->p_full[i], kCompute);
     mbar_init(&bars->ds_full[i], kCompute);
   }
   mbar_init(&bars->acc_full, 1);
@@ -189,32 +159,53 @@ __device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint32_t a_smem, int a
   }
 }
 
-// The 4 MMAs of acc (+)= A x B with A = 64 packed bf16 keys in TMEM and B =
-// [64 rows][D] in shared memory (MN-major, b_chunk-byte chunks).
-__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, int b_chunk,
-                                          uint32_t idesc, bool accumulate) {
-  const uint64_t b0 = sdesc_sw128(b_smem, b_chunk, 1024);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-    mma_ts(d_tmem, a_tmem + packed_slice_col(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
-}
+// TMEM column of 16-element slice kk (0..7) of a 128-element bf16 operand row
+// that the two compute halves packed: half h writes elements [64h, 64h + 64)
+// into columns [64h, 64h + 32).
+__device__ __forceinline__ uint32_t packed_slice_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 // ============================================================== dK / dV
+
+// dK/dV tiles: 128 key rows per CTA (K, V resident), 128-row query blocks
+// streamed, so every MMA runs at full rate (N = 128).  TMEM: S^T (128
+// columns), dP^T (128), dV (D), dK (D): at D = 128 there is no room for a
+// second score buffer, so the compute warps work in two passes per block
+// (P^T from S^T, then dS^T from dP^T) and the MMA warp queues
+//   dV(n) S^T(n+1) dK(n) dP^T(n+1) ...
+// so that each pass overlaps the MMAs of the other buffer.
+template <int D>
+struct DkdvTiles {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunk = 128 * kRowBytes;  // [128][64] bf16 = 16 KB
+  static constexpr int kTile = kChunks * kChunk;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kOffRes0 = 0;                      // K
+  static constexpr int kOffRes1 = kTile;                  // V
+  static constexpr int kOffX = 2 * kTile;                 // Q stages
+  static constexpr int kOffY = kOffX + kStages * kTile;   // dO stages
+  static constexpr int kOffRows = kOffY + kStages * kTile;  // [stage][LSE*log2e 128 | Delta 128]
+  static constexpr int kOffBar = kOffRows + kStages * 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmS = 0;     // S^T, then P^T (bf16)
+  static constexpr uint32_t kTmDP = 128;  // dP^T, then dS^T (bf16)
+  static constexpr uint32_t kTmDV = 256;
+  static constexpr uint32_t kTmDK = 256 + D;
+};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                             const BwdParams p) {
-  using C = Tiles<D>;
-  constexpr int BQ = 64;   // query rows per streamed block
+  using C = DkdvTiles<D>;
+  constexpr int BQ = 128;  // query rows per streamed block
   constexpr int BK = 128;  // key rows per CTA
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
-  float* srows = reinterpret_cast<float*>(smem + C::kOffRows);  // [stage][LSE*log2e 64 | Delta 64]
+  float* srows = reinterpret_cast<float*>(smem + C::kOffRows);
 
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
@@ -247,31 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kBigTile);
+      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kBigChunk, g * D + c * 64, kb * BK, b);
-        tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kBigChunk, g * D + c * 64, kb * BK, b);
+        tma_load_3d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, g * D + c * 64, kb * BK, b);
+        tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, g * D + c * 64, kb * BK, b);
       }
     }
     int issued = 0;
     for (int n = 0; n < niter; ++n) {
-      const int st = n % kStages;
-      if (n >= kStages && !warp_wait(&bars->x_empty[st], ((n / kStages) - 1) & 1, ctl, kCode)) break;
+      const int st = n % C::kStages;
+      if (n >= C::kStages && !warp_wait(&bars->x_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
       const int h = g * rep + n / nqb;
       const int qb = qlo + n % nqb;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kSmallTile);
+        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kSmallTile + c * C::kSmallChunk,
-                      h * D + c * 64, qb * BQ, b);
-          tma_load_3d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kSmallTile + c * C::kSmallChunk,
-                      h * D + c * 64, qb * BQ, b);
+          tma_load_3d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, h * D + c * 64,
+                      qb * BQ, b);
+          tma_load_3d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, h * D + c * 64,
+                      qb * BQ, b);
         }
       }
-      // LSE (pre-scaled to base 2) and Delta of the block's 64 query rows
-      float* rows = srows + st * 128;
+      // LSE (pre-scaled to base 2) and Delta of the block's 128 query rows
+      float* rows = srows + st * 256;
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < 4; ++k) {
         const int r = lane + 32 * k;
         const int i = qb * BQ + r;
         float l2 = 0.f, dl = 0.f;
@@ -281,51 +272,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           dl = p.Delta[idx];
         }
         rows[r] = l2;
-        rows[64 + r] = dl;
+        rows[128 + r] = dl;
       }
       mbar_arrive(&bars->x_full[st]);
       issued = n + 1;
     }
     if (lane == 0 && bars->abort) {
       drain_bar(&bars->res_full, 0, p.timeout_ns);
-      for (int n = imax(0, issued - kStages); n < issued; ++n)
-        drain_bar(&bars->x_full[n % kStages], (n / kStages) & 1, p.timeout_ns);
+      for (int n = imax(0, issued - C::kStages); n < issued; ++n)
+        drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BQ, false, false);  // K-major x K-major, N = 64
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BQ, false, false);  // K-major x K-major, N = 128
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sK = sbase + C::kOffRes0;
       const uint32_t sV = sbase + C::kOffRes1;
-      // S^T_n = K Q_n^T and dP^T_n = V dO_n^T into buffer n & 1
-      auto issue_sdp = [&](int n) -> bool {
-        const int st = n % kStages;
-        const int bf = n & 1;
-        if (!wait_bar(&bars->x_full[st], (n / kStages) & 1, ctl, kCode)) return false;
+      auto issue_s = [&](int n) -> bool {  // S^T_n = K Q_n^T
+        const int st = n % C::kStages;
+        if (!wait_bar(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
-        issue_kk<D>(tmem + C::kTmS + bf * 64, sK, C::kBigChunk, sbase + C::kOffX + st * C::kSmallTile,
-                    C::kSmallChunk, idesc_s);
-        mma_commit(&bars->s_full[bf]);
-        issue_kk<D>(tmem + C::kTmDP + bf * 64, sV, C::kBigChunk, sbase + C::kOffY + st * C::kSmallTile,
-                    C::kSmallChunk, idesc_s);
-        mma_commit(&bars->dp_full[bf]);
+        issue_kk<D>(tmem + C::kTmS, sK, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk, idesc_s);
+        mma_commit(&bars->s_full[0]);
         return true;
       };
+      auto issue_dp = [&](int n) {  // dP^T_n = V dO_n^T (stage already waited for by issue_s)
+        issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + (n % C::kStages) * C::kTile, C::kChunk,
+                    idesc_s);
+        mma_commit(&bars->dp_full[0]);
+      };
+      // acc (+)= A[TMEM, 128 packed query rows] x B[128 query rows][D] (MN-major)
+      auto issue_acc128 = [&](uint32_t acc, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
+        const uint64_t b0 = sdesc_sw128(b_smem, C::kChunk, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk)
+          mma_ts(acc, a_tmem + packed_slice_col128(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
       bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
-      if (ok && niter > 0) ok = issue_sdp(0);
+      if (ok && niter > 0) {
+        ok = issue_s(0);
+        if (ok) issue_dp(0);
+      }
       for (int n = 0; ok && n < niter; ++n) {
-        if (n + 1 < niter && !(ok = issue_sdp(n + 1))) break;
-        const int st = n % kStages;
-        const int bf = n & 1;
-        if (!(ok = wait_bar(&bars->ds_full[bf], (n >> 1) & 1, ctl, kCode))) break;
+        const int st = n % C::kStages;
+        if (!(ok = wait_bar(&bars->p_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (K = the block's 64 query rows)
-        issue_acc(tmem + C::kTmAcc, tmem + C::kTmS + bf * 64, sbase + C::kOffY + st * C::kSmallTile,
-                  C::kSmallChunk, idesc_acc, n > 0);
-        issue_acc(tmem + C::kTmAcc + D, tmem + C::kTmDP + bf * 64, sbase + C::kOffX + st * C::kSmallTile,
-                  C::kSmallChunk, idesc_acc, n > 0);
+        issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + st * C::kTile, n > 0);  // dV += P^T dO
+        if (n + 1 < niter && !(ok = issue_s(n + 1))) break;  // P^T_n is read by the dV MMAs queued above
+        if (!(ok = wait_bar(&bars->ds_full[0], n & 1, ctl, kCode))) break;
+        tc_fence_after();
+        issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + st * C::kTile, n > 0);  // dK += dS^T Q
         mma_commit(&bars->x_empty[st]);
+        if (n + 1 < niter) issue_dp(n + 1);  // dS^T_n is read by the dK MMAs queued above
       }
       if (ok) mma_commit(&bars->acc_full);
       mma_commit(&bars->drain);
@@ -334,59 +334,93 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- compute
     const int quarter = warp & 3;          // TMEM lane quarter
-    const int half = warp >> 2;            // 32-column half of each tile
+    const int half = warp >> 2;            // 64-column half of each 128-column tile
     const int jrow = quarter * 32 + lane;  // key row within the block (TMEM lane)
     const int j = kb * BK + jrow;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + C::kTmS + half * 64;
+    const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int n = 0; ok && n < niter; ++n) {
-      const int st = n % kStages;
-      const int bf = n & 1;
+      const int st = n % C::kStages;
       const int qb = qlo + n % nqb;
-      if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
-      if (!(ok = warp_wait(&bars->dp_full[bf], (n >> 1) & 1, ctl, kCode))) break;
-      if (!(ok = warp_wait(&bars->x_full[st], (n / kStages) & 1, ctl, kCode))) break;  // rows visible
+      const float* rows = srows + st * 256 + half * 64;
+      // pass 1: P^T = 2^(S^T*scale*log2e - LSE*log2e), masked -> bf16 over S^T
+      if (!(ok = warp_wait(&bars->s_full[0], n & 1, ctl, kCode))) break;
+      if (!(ok = warp_wait(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode))) break;  // rows visible
       tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 64 + half * 32;
-      const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + bf * 64 + half * 32;
-      float pv[32], ds[32];
-      load_two_cols32(s_addr, dp_addr, pv, ds);
-      const float4* lse4 = reinterpret_cast<const float4*>(srows + st * 128 + half * 32);
-      const float4* del4 = reinterpret_cast<const float4*>(srows + st * 128 + 64 + half * 32);
+      const bool need_mask = block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb);
+      float pv[64];
+      {
+        float lo[32], hi[32];
+        load_two_cols32(s_addr, s_addr + 32, lo, hi);
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
+        for (int c = 0; c < 32; ++c) {
+          pv[c] = lo[c];
+          pv[32 + c] = hi[c];
+        }
+      }
+      const float4* lse4 = reinterpret_cast<const float4*>(rows);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l = lse4[c4];
-        const float4 d = del4[c4];
         pv[4 * c4 + 0] = ex2(fmaf(pv[4 * c4 + 0], sl2, -l.x));
         pv[4 * c4 + 1] = ex2(fmaf(pv[4 * c4 + 1], sl2, -l.y));
         pv[4 * c4 + 2] = ex2(fmaf(pv[4 * c4 + 2], sl2, -l.z));
         pv[4 * c4 + 3] = ex2(fmaf(pv[4 * c4 + 3], sl2, -l.w));
-        ds[4 * c4 + 0] -= d.x;
-        ds[4 * c4 + 1] -= d.y;
-        ds[4 * c4 + 2] -= d.z;
-        ds[4 * c4 + 3] -= d.w;
       }
-      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
-        const int i0 = qb * BQ + half * 32;
+      if (need_mask) {
+        const int i0 = qb * BQ + half * 64;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
+        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
       }
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) ds[c] *= pv[c];  // dS^T = P^T (dP^T - Delta)
-      store_cols32_bf16(s_addr, pv);
-      store_cols32_bf16(dp_addr, ds);
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        tmem_st32(s_addr, pk);  // 64 packed values into the first 32 columns of this half
+      }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full[bf]);
+      mbar_arrive(&bars->p_full[0]);
+      // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T
+      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
+      tc_fence_after();
+      float dlo[32], dhi[32];
+      load_two_cols32(dp_addr, dp_addr + 32, dlo, dhi);
+      const float4* del4 = reinterpret_cast<const float4*>(rows + 128);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 d = del4[c4];
+        const float4 e = del4[8 + c4];
+        dlo[4 * c4 + 0] = pv[4 * c4 + 0] * (dlo[4 * c4 + 0] - d.x);
+        dlo[4 * c4 + 1] = pv[4 * c4 + 1] * (dlo[4 * c4 + 1] - d.y);
+        dlo[4 * c4 + 2] = pv[4 * c4 + 2] * (dlo[4 * c4 + 2] - d.z);
+        dlo[4 * c4 + 3] = pv[4 * c4 + 3] * (dlo[4 * c4 + 3] - d.w);
+        dhi[4 * c4 + 0] = pv[32 + 4 * c4 + 0] * (dhi[4 * c4 + 0] - e.x);
+        dhi[4 * c4 + 1] = pv[32 + 4 * c4 + 1] * (dhi[4 * c4 + 1] - e.y);
+        dhi[4 * c4 + 2] = pv[32 + 4 * c4 + 2] * (dhi[4 * c4 + 2] - e.z);
+        dhi[4 * c4 + 3] = pv[32 + 4 * c4 + 3] * (dhi[4 * c4 + 3] - e.w);
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        pk[e] = pack_bf16x2(dlo[2 * e], dlo[2 * e + 1]);
+        pk[16 + e] = pack_bf16x2(dhi[2 * e], dhi[2 * e + 1]);
+      }
+      tmem_st32(dp_addr, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full[0]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D + half * (D / 2);
-      store_acc_row(tmem + lane_addr + C::kTmAcc + half * (D / 2), D / 2, 1.f,
+      store_acc_row(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, 1.f,
                     static_cast<__nv_bfloat16*>(p.dV) + rowoff, j < s.T);
-      store_acc_row(tmem + lane_addr + C::kTmAcc + D + half * (D / 2), D / 2, s.scale,
+      store_acc_row(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, s.scale,
                     static_cast<__nv_bfloat16*>(p.dK) + rowoff, j < s.T);
     }
   }
@@ -423,11 +457,6 @@ struct DqTiles {
   static constexpr uint32_t kTmDP = 256;  // 128 columns
   static constexpr uint32_t kTmDQ = 384;  // D columns
 };
-
-// TMEM column of 16-key slice kk (0..7) of a 128-key bf16 dS row that the two
-// compute halves packed: half h writes keys [64h, 64h + 64) into columns
-// [64h, 64h + 32).
-__device__ __forceinline__ uint32_t packed_slice_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -605,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  using C = Tiles<D>;
+  using C = DkdvTiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -614,7 +643,7 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
     attr_set = true;
   }
   dim3 grid(ceil_div(p.s.T, 128), p.s.HKV, p.s.B);
-  fa_bwd_dkdv_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q64, tm.k, tm.v, tm.dO64, p);
+  fa_bwd_dkdv_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }
 
