@@ -5,7 +5,8 @@
 // One CTA computes one 128-row query tile of one (b, h).  Warp roles:
 //   warps 0-3  softmax: thread t owns query row t of the tile (= TMEM lane t).
 //   warp  4    TMA producer: the Q tile once, then K and V blocks through an
-//              NS-stage ring guarded by full/empty mbarriers.
+//              NS-stage ring guarded by full/empty mbarriers (a K stage is
+//              released as soon as its S MMA is done, a V stage after PV).
 //   warp  5    MMA issuer (one thread) and TMEM owner.
 //
 // Per visible KV block n (the loop skips blocks above the causal diagonal and
@@ -37,7 +38,7 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;              // 64-wide bf16 chunks per row
   static constexpr int kChunkBytes = 128 * 64 * 2;    // one [128][64] chunk
   static constexpr int kTileBytes = kChunks * kChunkBytes;
-  static constexpr int kStages = (D == 64) ? 4 : 2;   // K/V ring depth
+  static constexpr int kStages = (D == 64) ? 4 : 3;   // K/V ring depth (3 x 64 KB fits at D = 128)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
@@ -57,7 +58,8 @@ struct Bars {
   uint64_t q_tmem;  // Q copied into TMEM by the 128 softmax threads
   uint64_t k_full[4];
   uint64_t v_full[4];
-  uint64_t kv_empty[4];
+  uint64_t k_empty[4];  // K stage free once its S MMA completed
+  uint64_t v_empty[4];  // V stage free once its PV MMA completed
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done;
@@ -114,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -148,13 +151,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
         const int st = n % C::kStages;
-        if (n >= C::kStages && !wait_bar(&bars->kv_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
         const int kb = kb_lo + n;
         uint8_t* sk = smem + C::kOffK + st * C::kTileBytes;
         uint8_t* sv = smem + C::kOffV + st * C::kTileBytes;
+        if (n >= C::kStages && !wait_bar(&bars->k_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+        if (n >= C::kStages && !wait_bar(&bars->v_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) {
+          drain_bar(&bars->k_full[st], (n / C::kStages) & 1, p.timeout_ns);
+          break;
+        }
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
@@ -182,13 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar(&bars->k_full[st], (n / C::kStages) & 1, ctl, kCode))) break;
           tc_fence_after();
           const uint32_t sk = sbase + C::kOffK + st * C::kTileBytes;
+          // descriptors built once, stepped by (bytes >> 4) in the address field
+          const uint64_t kdesc = sdesc_sw128(sk, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ts(tmem + C::kTmS + sb * 128, tmem + C::kTmQ + kk * 8, sdesc_sw128(sk + off, 16, 1024), idesc_s,
-                   kk > 0);
+            const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ts(tmem + C::kTmS + sb * 128, tmem + C::kTmQ + kk * 8, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
           }
           mma_commit(&bars->s_full[sb]);
+          mma_commit(&bars->k_empty[st]);
         }
         if (n >= 1) {
           const int m = n - 1;
@@ -198,14 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_bar(&bars->v_full[st], (m / C::kStages) & 1, ctl, kCode))) break;
           tc_fence_after();
           const uint32_t sv = sbase + C::kOffV + st * C::kTileBytes;
+          const uint64_t vdesc = sdesc_sw128(sv, C::kChunkBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             // P: 16 bf16 keys per step = 8 TMEM columns; V: 16 key rows = 2048 bytes
-            mma_ts(tmem + C::kTmO, tmem + C::kTmS + sb * 128 + kk * 8,
-                   sdesc_sw128(sv + kk * 2048, C::kChunkBytes, 1024), idesc_o, (m > 0 || kk > 0));
+            mma_ts(tmem + C::kTmO, tmem + C::kTmS + sb * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
+                   (m > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&bars->o_done);
-          mma_commit(&bars->kv_empty[st]);
+          mma_commit(&bars->v_empty[st]);
         }
       }
       // every MMA this thread issued must finish before TMEM is released
