@@ -180,18 +180,21 @@ class ClockSampler:
 
 # -------------------------------------------------------------- CPU baseline
 
-def cpu_sample_workload(w: Workload, T: int) -> Workload:
-    """One query head (and its KV head) of the workload over its first T
-    positions: same recipe and value distributions, bounded size."""
-    return w.replace(B=1, H=1, HKV=1, T=T, window=min(w.window, T) if w.window else 0)
+def cpu_sample_workload(w: Workload, T: int, heads: int = 0) -> Workload:
+    """One KV head and `heads` of its query heads (default: its whole group)
+    of the workload over its first T positions: same recipe and value
+    distributions, bounded size."""
+    rep = w.H // w.HKV
+    hq = heads if heads > 0 else rep
+    return w.replace(B=1, H=hq, HKV=1, T=T, window=min(w.window, T) if w.window else 0)
 
 
-def cpu_sample_run(wid: int, T: int, steps: int) -> dict:
+def cpu_sample_run(wid: int, T: int, steps: int, heads: int = 0) -> dict:
     """Time the fp64 oracle (fwd + bwd) on the bounded sample; one run per step."""
     import oracle
     from flash_attention_attn_gb300.inputs import as_f64
 
-    w = cpu_sample_workload(WORKLOADS[wid], T)
+    w = cpu_sample_workload(WORKLOADS[wid], T, heads)
     inp = make_inputs(w)
     Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
     oracle.build()
@@ -201,15 +204,15 @@ def cpu_sample_run(wid: int, T: int, steps: int) -> dict:
         oracle.fwd(Q, K, V, w.scale, w.causal, w.window)
         oracle.bwd(Q, K, V, dO, w.scale, w.causal, w.window)
         times.append(time.perf_counter() - t0)
-    return {"seconds": times, "flops": counted_flops(w)["fwd_bwd"], "T": T}
+    return {"seconds": times, "flops": counted_flops(w)["fwd_bwd"], "T": T, "heads": w.H}
 
 
-def cpu_baseline(wid: int, T: int, steps: int = 1) -> dict:
+def cpu_baseline(wid: int, T: int, steps: int = 1, heads: int = 0) -> dict:
     """Run cpu_sample_run in a fresh process with OpenMP over every core we may use."""
     cores = len(os.sched_getaffinity(0))
     env = dict(os.environ, OMP_NUM_THREADS=str(cores), OMP_PROC_BIND="false")
     code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench.cpu_sample_run(%d, %d, %d)))" % (ROOT, wid, T, steps))
+            "print(json.dumps(bench.cpu_sample_run(%d, %d, %d, %d)))" % (ROOT, wid, T, steps, heads))
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError(f"cpu baseline failed: {r.stderr[-2000:]}")
@@ -397,7 +400,7 @@ def main():
         # the reference arm is the fp64 oracle on the host cores, rank 0 only
         if rank != 0:
             return
-        s = cpu_baseline(w.wid, args.ref_T, steps=args.warmup + args.steps)
+        s = cpu_baseline(w.wid, args.ref_T, steps=args.warmup + args.steps, heads=1)
         times = s["seconds"][args.warmup:]
         tot = sum(times)
         val = len(times) * s["flops"] / tot / 1e12
@@ -484,8 +487,8 @@ def main():
         line["cpu_baseline"] = {
             "value": cpu["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": cpu["cores"], "kind": "oracle",
             "seconds": t,
-            "sample": (f"fp64 oracle fwd+bwd of one query head of '{w.name}' over its first {cpu['T']} "
-                       f"positions ({cpu['flops'] / 1e9:.1f} GFLOP counted)")}
+            "sample": (f"fp64 oracle fwd+bwd of one KV head and its {cpu['heads']} query heads of '{w.name}' "
+                       f"over the first {cpu['T']} positions ({cpu['flops'] / 1e9:.1f} GFLOP counted)")}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
