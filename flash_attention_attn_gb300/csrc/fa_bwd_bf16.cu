@@ -83,14 +83,6 @@ __device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float 
   }
 }
 
-// 32 values as 16 packed bf16x2 columns at taddr.
-__device__ __forceinline__ void store_cols32_bf16(uint32_t taddr, const float (&v)[32]) {
-  uint32_t pk[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-  tmem_st16(taddr, pk);
-}
-
 // Write `ncols` fp32 TMEM columns of this thread's lane, times `mul`, as bf16
 // to global memory at dst (16-byte aligned, ncols a multiple of 32).
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, __nv_bfloat16* dst,
@@ -113,8 +105,10 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
 
 struct BwdBars {
   uint64_t res_full;
-  uint64_t x_full[kStages];
-  uint64_t x_empty[kStages];
+  uint64_t x_full[kStages];   // streamed stage (K in dQ) loaded
+  uint64_t x_empty[kStages];  // streamed stage (K in dQ) free
+  uint64_t v_full[kStages];   // dQ only: V stage loaded
+  uint64_t v_empty[kStages];  // dQ only: V stage free
   uint64_t s_full[2];
   uint64_t dp_full[2];
   uint64_t p_full[2];   // P written back (256 compute threads)
@@ -130,6 +124,8 @@ __device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) 
   for (int i = 0; i < kStages; ++i) {
     mbar_init(&bars->x_full[i], x_full_count);
     mbar_init(&bars->x_empty[i], 1);
+    mbar_init(&bars->v_full[i], 1);
+    mbar_init(&bars->v_empty[i], 1);
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bars->s_full[i], 1);
@@ -445,12 +441,15 @@ struct DqTiles {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunk = 128 * kRowBytes;  // [128][64] bf16 = 16 KB
   static constexpr int kTile = kChunks * kChunk;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  // K is held from its S MMA to its dQ MMA, V only until its dP MMA: K gets
+  // the deeper ring (3 + 2 stages = 224 KB of tiles at D = 128)
+  static constexpr int kKStages = (D == 64) ? 4 : 3;
+  static constexpr int kVStages = (D == 64) ? 4 : 2;
   static constexpr int kOffRes0 = 0;               // Q
   static constexpr int kOffRes1 = kTile;           // dO
-  static constexpr int kOffX = 2 * kTile;          // K stages
-  static constexpr int kOffY = kOffX + kStages * kTile;  // V stages
-  static constexpr int kOffBar = kOffY + kStages * kTile;
+  static constexpr int kOffK = 2 * kTile;          // K stages
+  static constexpr int kOffV = kOffK + kKStages * kTile;  // V stages
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmS = 0;     // 2 x 128 columns
@@ -496,6 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr unsigned kCode = 4u;  // FA_DEVERR_DQ_TIMEOUT
 
   if (warp == 8) {
+    // lane 0 streams K (and loads Q, dO once), lane 1 streams V: separate
+    // rings, so a V wait never holds back the next K load
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
@@ -508,23 +509,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
-        const int st = n % C::kStages;
-        if (n >= C::kStages && !wait_bar(&bars->x_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
-        const int kb = kb_lo + n;
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTile);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, g * D + c * 64,
-                      kb * BK, b);
-          tma_load_3d(&tmV, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, g * D + c * 64,
-                      kb * BK, b);
-        }
+        const int st = n % C::kKStages;
+        if (n >= C::kKStages && !wait_bar(&bars->x_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx(&bars->x_full[st], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffK + st * C::kTile + c * C::kChunk, g * D + c * 64,
+                      (kb_lo + n) * BK, b);
         issued = n + 1;
       }
       if (bars->abort) {
         drain_bar(&bars->res_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued - C::kStages); n < issued; ++n)
-          drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
+        for (int n = imax(0, issued - C::kKStages); n < issued; ++n)
+          drain_bar(&bars->x_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
       }
+    } else if (lane == 1) {
+      int issued = 0;
+      for (int n = 0; n < nblk; ++n) {
+        const int st = n % C::kVStages;
+        if (n >= C::kVStages && !wait_bar(&bars->v_empty[st], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmV, &bars->v_full[st], smem + C::kOffV + st * C::kTile + c * C::kChunk, g * D + c * 64,
+                      (kb_lo + n) * BK, b);
+        issued = n + 1;
+      }
+      if (bars->abort)
+        for (int n = imax(0, issued - C::kVStages); n < issued; ++n)
+          drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     if (lane == 0) {
@@ -533,33 +544,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sQ = sbase + C::kOffRes0;
       const uint32_t sdO = sbase + C::kOffRes1;
       auto issue_s = [&](int n) -> bool {  // S_n = Q K_n^T into buffer n & 1
-        const int st = n % C::kStages;
-        if (!wait_bar(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
+        const int st = n % C::kKStages;
+        if (!wait_bar(&bars->x_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
-        issue_kk<D>(tmem + C::kTmS + (n & 1) * 128, sQ, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk,
+        issue_kk<D>(tmem + C::kTmS + (n & 1) * 128, sQ, C::kChunk, sbase + C::kOffK + st * C::kTile, C::kChunk,
                     idesc_s);
         mma_commit(&bars->s_full[n & 1]);
         return true;
       };
-      auto issue_dp = [&](int n) {  // dP_n = dO V_n^T (its stage was waited for by issue_s)
-        issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffY + (n % C::kStages) * C::kTile, C::kChunk,
-                    idesc_s);
+      auto issue_dp = [&](int n) -> bool {  // dP_n = dO V_n^T; its V stage is free once this completes
+        const int st = n % C::kVStages;
+        if (!wait_bar(&bars->v_full[st], (n / C::kVStages) & 1, ctl, kCode)) return false;
+        tc_fence_after();
+        issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffV + st * C::kTile, C::kChunk, idesc_s);
         mma_commit(&bars->dp_full[0]);
+        mma_commit(&bars->v_empty[st]);
+        return true;
       };
       bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
       if (ok && nblk > 0) {
         ok = issue_s(0);
-        if (ok) issue_dp(0);
+        if (ok) ok = issue_dp(0);
       }
       // queue order: S0 dP0 S1 | dP1 dQ0 S2 | dP2 dQ1 S3 ...
       for (int n = 0; ok && n < nblk; ++n) {
         if (n + 1 < nblk && !(ok = issue_s(n + 1))) break;
-        const int st = n % C::kStages;
+        const int st = n % C::kKStages;
         if (!(ok = wait_bar(&bars->ds_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
-        if (n + 1 < nblk) issue_dp(n + 1);  // dP_n has been read: its columns are free
+        if (n + 1 < nblk && !(ok = issue_dp(n + 1))) break;  // dP_n has been read: its columns are free
         // dQ += dS K   (K = the block's 128 key rows)
-        const uint64_t b0 = sdesc_sw128(sbase + C::kOffX + st * C::kTile, C::kChunk, 1024);
+        const uint64_t b0 = sdesc_sw128(sbase + C::kOffK + st * C::kTile, C::kChunk, 1024);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma_ts(tmem + C::kTmDQ, tmem + C::kTmS + (n & 1) * 128 + packed_slice_col128(kk),
@@ -587,28 +602,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; ok && n < nblk; ++n) {
       const int kb = kb_lo + n;
       const int bf = n & 1;
+      // pass 1 (overlaps the dP MMA of this block): P = 2^(S*scale*log2e - LSE*log2e), masked
       if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
-      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 128 + half * 64;
       const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
-      const bool need_mask = block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb);
+      float pv[64];
+      {
+        float lo[32], hi[32];
+        load_two_cols32(s_addr, s_addr + 32, lo, hi);
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {  // 32 keys at a time
-        float pv[32], ds[32];
-        load_two_cols32(s_addr + part * 32, dp_addr + part * 32, pv, ds);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pv[c] = ex2(fmaf(pv[c], sl2, -lse2));
-        if (need_mask) {
-          const int j0 = kb * BK + half * 64 + part * 32;
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+        for (int c = 0; c < 32; ++c) {
+          pv[c] = ex2(fmaf(lo[c], sl2, -lse2));
+          pv[32 + c] = ex2(fmaf(hi[c], sl2, -lse2));
         }
+      }
+      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
+        const int j0 = kb * BK + half * 64;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) ds[c] = pv[c] * (ds[c] - delta);  // dS = P (dP - Delta)
-        // packed dS of keys [32 part, 32 part + 32) into columns [16 part, 16 part + 16)
-        // of this half's region (already read)
-        store_cols32_bf16(s_addr + part * 16, ds);
+        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+      }
+      // pass 2: dS = P (dP - Delta) -> bf16 over the S columns this thread read
+      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
+      tc_fence_after();
+      {
+        float lo[32], hi[32];
+        load_two_cols32(dp_addr, dp_addr + 32, lo, hi);
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack_bf16x2(pv[2 * e] * (lo[2 * e] - delta), pv[2 * e + 1] * (lo[2 * e + 1] - delta));
+          pk[16 + e] = pack_bf16x2(pv[32 + 2 * e] * (hi[2 * e] - delta), pv[33 + 2 * e] * (hi[2 * e + 1] - delta));
+        }
+        tmem_st32(s_addr, pk);  // dS of keys [64 half, 64 half + 64) -> columns [64 half, 64 half + 32)
       }
       tmem_st_wait();
       tc_fence_before();
