@@ -52,14 +52,6 @@ constexpr int kStages = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kRowBytes = 128;  // one 64-element bf16 row of a swizzled chunk
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& ctl, unsigned code) {
-  bool ok = false;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, ctl, code);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
-}
-
 __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),

@@ -68,16 +68,6 @@ struct Bars {
   int abort;
 };
 
-// Lane 0 waits, the warp follows its verdict (keeps .sync.aligned tcgen05
-// instructions convergent even when a wait gives up).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& ctl, unsigned code) {
-  bool ok = false;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, ctl, code);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
-}
-
 __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
   asm volatile(""
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),

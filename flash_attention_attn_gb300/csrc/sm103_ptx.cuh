@@ -88,6 +88,16 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const C
   }
 }
 
+// Warp-wide wait: every lane polls the barrier (one warp-wide try_wait per
+// poll) and the warp returns the common verdict, so the .sync.aligned tcgen05
+// instructions that follow stay convergent even when a wait gives up.  Polling
+// from lane 0 alone, with the other lanes parked at a shuffle, was measured
+// on GB300 to add several hundred cycles to every handoff.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Ctl& ctl, unsigned int code) {
+  const bool ok = wait_bar(bar, parity, ctl, code);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Same, but ignores the abort flag: used only to drain copies already in
 // flight before a CTA that aborted exits.
 __device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
