@@ -232,6 +232,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, g * D + c * 64, kb * BK, b);
       }
     }
+    // LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
+    // four per lane; read one block ahead so that their latency overlaps the
+    // wait for the stage
+    float l2[4], dl[4];
+    auto load_rows = [&](int n) {
+      const int h = g * rep + n / nqb;
+      const int qb = qlo + n % nqb;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = qb * BQ + lane + 32 * k;
+        l2[k] = 0.f;
+        dl[k] = 0.f;
+        if (i < s.T) {
+          const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
+          l2[k] = p.LSE[idx] * kLog2e;
+          dl[k] = p.Delta[idx];
+        }
+      }
+    };
+    if (niter > 0) load_rows(0);
     int issued = 0;
     for (int n = 0; n < niter; ++n) {
       const int st = n % C::kStages;
@@ -247,23 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                       qb * BQ, b);
         }
       }
-      // LSE (pre-scaled to base 2) and Delta of the block's 128 query rows
       float* rows = srows + st * 256;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int r = lane + 32 * k;
-        const int i = qb * BQ + r;
-        float l2 = 0.f, dl = 0.f;
-        if (i < s.T) {
-          const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
-          l2 = p.LSE[idx] * kLog2e;
-          dl = p.Delta[idx];
-        }
-        rows[r] = l2;
-        rows[128 + r] = dl;
+        rows[lane + 32 * k] = l2[k];
+        rows[128 + lane + 32 * k] = dl[k];
       }
       mbar_arrive(&bars->x_full[st]);
       issued = n + 1;
+      if (n + 1 < niter) load_rows(n + 1);
     }
     if (lane == 0 && bars->abort) {
       drain_bar(&bars->res_full, 0, p.timeout_ns);
