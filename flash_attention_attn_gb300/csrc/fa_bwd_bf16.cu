@@ -122,8 +122,8 @@ __device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) 
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bars->s_full[i], 1);
     mbar_init(&bars->dp_full[i], 1);
-    mbar_init(&bars->p_full[i], kCompute);
-    mbar_init(&bars->ds_full[i], kCompute);
+    mbar_init(&bars->p_full[i], kCompute / 32);  // one arrival per compute warp
+    mbar_init(&bars->ds_full[i], kCompute / 32);
   }
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->drain, 1);
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->p_full[0]);
+      warp_arrive(&bars->p_full[0]);
       // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T
       if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
       tc_fence_after();
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(dp_addr, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full[0]);
+      warp_arrive(&bars->ds_full[0]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->ds_full[0]);
+      warp_arrive(&bars->ds_full[0]);
     }
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->q_tmem, 128);
+    mbar_init(&bars->q_tmem, 4);
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->v_full[i], 1);
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], 128);
+      mbar_init(&bars->p_full[i], 4);  // one arrival per softmax warp
     }
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->drain, 1);
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tile_row_to_tmem<D>(smem + C::kOffQ, C::kChunkBytes, t, tmem + lane_addr + C::kTmQ);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->q_tmem);
+      warp_arrive(&bars->q_tmem);
     }
     for (int n = 0; ok && n < nblk; ++n) {
       const int kb = kb_lo + n;
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (first || resc) m_run = m_new;
       l_run += sum;
       tc_fence_before();
-      mbar_arrive(&bars->p_full[sb]);
+      warp_arrive(&bars->p_full[sb]);
     }
     if (ok && nblk > 0) ok = warp_wait(&bars->o_done, (nblk - 1) & 1, ctl, kCode);
     if (ok) {

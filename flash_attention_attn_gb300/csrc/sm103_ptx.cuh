@@ -98,6 +98,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xffffffffu, ok);
 }
 
+// One arrival per warp on a barrier initialised with the number of arriving
+// warps: each lane has already waited for and fenced its own tcgen05 stores,
+// the warp syncs, lane 0 arrives.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Same, but ignores the abort flag: used only to drain copies already in
 // flight before a CTA that aborted exits.
 __device__ __forceinline__ bool drain_bar(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
