@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     fa_bwd_preprocess,
     fa_check_status,
     fa_debug_config,
+    fa_debug_fwd_tiles,
     fa_fwd,
     fa_plan_block_mask,
     fa_plan_kv_range,

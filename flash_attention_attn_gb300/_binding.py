@@ -88,6 +88,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_tile_n.restype = _i
         lib.fa_debug_config.argtypes = [ctypes.c_ulonglong, _i]
         lib.fa_debug_config.restype = _i
+        lib.fa_debug_fwd_tiles.argtypes = [_i]
+        lib.fa_debug_fwd_tiles.restype = _i
         _lib = lib
         return lib
 
@@ -169,6 +171,10 @@ def fa_tile_n() -> int:
 
 def fa_debug_config(wait_timeout_ns: int = 0, inject_stall: int = 0) -> int:
     return load().fa_debug_config(int(wait_timeout_ns), int(inject_stall))
+
+
+def fa_debug_fwd_tiles(tiles: int = 0) -> int:
+    return load().fa_debug_fwd_tiles(int(tiles))
 
 
 # ------------------------------------------------------------ torch layer

@@ -22,6 +22,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 std::atomic<unsigned long long> g_wait_ns{fa::kDefaultWaitNs};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_fwd_tiles{0};  // 0 = automatic
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -100,6 +101,14 @@ int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int 
 int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 }  // namespace
+
+namespace fa {
+bool fwd_two_tiles(const Shape& s) {
+  const int forced = g_fwd_tiles.load();
+  if (forced != 0) return forced == 2;
+  return ceil_div(s.T, kBM) >= 2;
+}
+}  // namespace fa
 
 extern "C" {
 
@@ -310,6 +319,12 @@ int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, in
 
 int fa_tile_m(void) { return fa::kBM; }
 int fa_tile_n(void) { return fa::kBN; }
+
+int fa_debug_fwd_tiles(int tiles) {
+  if (tiles < 0 || tiles > 2) return FA_ERR_INVALID_ARG;
+  g_fwd_tiles.store(tiles);
+  return FA_OK;
+}
 
 int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall) {
   g_wait_ns.store(wait_timeout_ns ? wait_timeout_ns : fa::kDefaultWaitNs);

@@ -342,6 +342,362 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- two tiles
+//
+// Two 128-row query tiles A and B (query blocks 2j and 2j + 1) of one (b, h)
+// per CTA, sharing every K/V block the CTA streams: each 64 KB K/V block
+// (D = 128) feeds four 128x128 MMA groups instead of two, which halves the
+// TMA traffic per MMA.  Measured on GB300, a K/V ring feeding one tile is
+// bounded near 1600 cycles per block by the TMA stream itself against 1024
+// cycles of MMAs.
+//   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B (warp w owns
+//             TMEM lanes 32*(w%4).. = rows of its tile)
+//   warp  8   TMA (lane 0): Q_A, Q_B, then K and V blocks in the order the
+//             MMAs need them
+//   warp  9   MMA issuer (lane 0) and TMEM owner
+// TMEM: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
+// No S buffer is doubled; the tiles ping-pong instead.  Per streamed block n
+// the MMA queue is  PV_A(n) S_A(n+1) PV_B(n) S_B(n+1), so the softmax of one
+// tile runs while the tensor pipe works on the other's.  S_t(n+1) overwrites
+// the P_t(n) that PV_t(n) reads; the tensor pipe executes in order.
+// A tile skips the streamed blocks outside its own visible range (with a
+// window the first block may be A's only, with causal masking the last is
+// B's only).
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 64 * 2;  // one [128][64] bf16 chunk
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  // a K stage is held from S_A(n) to S_B(n), a V stage from PV_A(n) to PV_B(n)
+  // one MMA iteration later, so V gets the deeper ring
+  static constexpr int kKStages = (D == 64) ? 4 : 2;
+  static constexpr int kVStages = (D == 64) ? 4 : 3;
+  static constexpr int kOffQ = 0;  // Q_A, Q_B
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmS = 0;    // S_t at t * 128
+  static constexpr uint32_t kTmO = 256;  // O_t at 256 + t * D
+};
+
+constexpr int kThreads2 = 320;
+
+struct Bars2 {
+  uint64_t q_full;
+  uint64_t k_full[4];
+  uint64_t k_empty[4];  // K stage free once the S MMAs of both tiles completed
+  uint64_t v_full[4];
+  uint64_t v_empty[4];  // V stage free once the PV MMAs of both tiles completed
+  uint64_t s_full[2];   // per tile
+  uint64_t p_full[2];   // per tile: one arrival per softmax warp
+  uint64_t o_done[2];   // per tile: its last PV MMA completed
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads2, 1)
+    fa_fwd2_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Fwd2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  Bars2* bars = reinterpret_cast<Bars2*>(smem + C::kOffBar);
+
+  const Shape& s = p.s;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nq = ceil_div(s.T, kBM);
+  const int npair = ceil_div(nq, 2);
+  const int pair = npair - 1 - static_cast<int>(blockIdx.x);  // longest causal pairs first
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int g = h / (s.H / s.HKV);
+  // visible KV block range of each tile (B is empty past the end)
+  int lo_a, hi_a, lo_b = 1, hi_b = 0;
+  kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, 2 * pair, lo_a, hi_a);
+  if (2 * pair + 1 < nq) kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, 2 * pair + 1, lo_b, hi_b);
+  const bool has_b = lo_b <= hi_b;
+  const int lo = has_b ? imin(lo_a, lo_b) : lo_a;
+  const int hi = has_b ? imax(hi_a, hi_b) : hi_a;
+  const int nblk = hi - lo + 1;  // the adjacent tiles' ranges overlap or touch: the union is contiguous
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->k_empty[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      mbar_init(&bars->v_empty[i], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->o_done[t], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const Ctl ctl{&bars->abort, p.err, p.timeout_ns};
+  constexpr unsigned kCode = 1u;  // FA_DEVERR_FWD_TIMEOUT
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && !p.inject_stall) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
+      for (int t = 0; t < (has_b ? 2 : 1); ++t)
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, h * D + c * 64,
+                      (2 * pair + t) * kBM, b);
+      int issued_k = 0, issued_v = 0;
+      for (int n = 0; n < nblk; ++n) {
+        const int st = n % C::kKStages;
+        if (n >= C::kKStages && !wait_bar(&bars->k_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
+                      g * D + c * 64, (lo + n) * kBN, b);
+        issued_k = n + 1;
+        const int sv = n % C::kVStages;
+        if (n >= C::kVStages && !wait_bar(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx(&bars->v_full[sv], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
+                      g * D + c * 64, (lo + n) * kBN, b);
+        issued_v = n + 1;
+      }
+      if (bars->abort) {
+        // let every copy already issued land before the CTA exits
+        drain_bar(&bars->q_full, 0, p.timeout_ns);
+        for (int n = imax(0, issued_k - C::kKStages); n < issued_k; ++n)
+          drain_bar(&bars->k_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
+        for (int n = imax(0, issued_v - C::kVStages); n < issued_v; ++n)
+          drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
+      }
+    }
+  } else if (warp == 9) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // Q x K^T, both K-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);     // P (TMEM) x V (MN-major)
+      int n_s[2] = {0, 0};  // S MMAs issued per tile (s_full phases)
+      int n_p[2] = {0, 0};  // PV MMAs issued per tile (p_full phases)
+      auto in_tile = [&](int t, int kb) { return t ? (lo_b <= kb && kb <= hi_b) : (lo_a <= kb && kb <= hi_a); };
+      auto issue_s = [&](int t, int n) -> bool {  // S_t = Q_t K_n^T
+        const int st = n % C::kKStages;
+        if (!wait_bar(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
+        tc_fence_after();
+        const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
+        const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kTmS + t * 128, qdesc + off, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bars->s_full[t]);
+        ++n_s[t];
+        return true;
+      };
+      bool ok = wait_bar(&bars->q_full, 0, ctl, kCode);
+      if (ok && nblk > 0) {
+        for (int t = 0; ok && t < 2; ++t)
+          if (in_tile(t, lo)) ok = issue_s(t, 0);
+        if (ok) mma_commit(&bars->k_empty[0]);
+      }
+      for (int n = 0; ok && n < nblk; ++n) {
+        const int kb = lo + n;
+        const int stv = n % C::kVStages;
+        if (!(ok = wait_bar(&bars->v_full[stv], (n / C::kVStages) & 1, ctl, kCode))) break;
+        const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + stv * C::kTileBytes, C::kChunkBytes, 1024);
+        for (int t = 0; ok && t < 2; ++t) {
+          if (in_tile(t, kb)) {
+            if (!(ok = wait_bar(&bars->p_full[t], n_p[t] & 1, ctl, kCode))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
+              mma_ts(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
+                     (n_p[t] > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&bars->o_done[t]);
+            ++n_p[t];
+          }
+          if (n + 1 < nblk && in_tile(t, kb + 1)) ok = issue_s(t, n + 1);
+        }
+        if (!ok) break;
+        mma_commit(&bars->v_empty[stv]);
+        if (n + 1 < nblk) mma_commit(&bars->k_empty[(n + 1) % C::kKStages]);
+      }
+      // every MMA this thread issued must finish before TMEM is released
+      mma_commit(&bars->drain);
+      drain_bar(&bars->drain, 0, p.timeout_ns);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax
+    const int t = warp >> 2;   // tile
+    const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
+    const int q = 2 * pair + t;
+    const int row = q * kBM + r;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem + lane_addr + C::kTmS + t * 128;
+    const uint32_t o_addr = tmem + lane_addr + C::kTmO + t * D;
+    const float sl2 = p.scale_log2;
+    const int lo_own = t ? lo_b : lo_a;
+    const int nb = (t ? hi_b : hi_a) - lo_own + 1;  // 0 for a tile past the end
+    float m_run = -CUDART_INF_F;  // reference max, log2 domain
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; ok && j < nb; ++j) {
+      const int kb = lo_own + j;
+      if (!(ok = warp_wait(&bars->s_full[t], j & 1, ctl, kCode))) break;
+      tc_fence_after();
+      // The loops below are kept rolled over 32-column chunks: fully unrolled,
+      // this softmax did not fit the instruction cache next to the other
+      // roles and ran several times slower.
+      if (block_needs_mask(s.T, kBM, kBN, s.causal, s.window, q, kb)) {
+        // rare (diagonal, window-edge and tail blocks): -inf over the masked
+        // scores in TMEM, so that both passes below stay mask-free
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t ra[32];
+          tmem_ld32(s_addr + c4 * 32, ra);
+          tmem_ld_wait(ra);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (masked(s.T, s.causal, s.window, row, kb * kBN + c4 * 32 + c)) ra[c] = __float_as_uint(-CUDART_INF_F);
+          tmem_st32(s_addr + c4 * 32, ra);
+        }
+        tmem_st_wait();
+      }
+      // pass 1: row max over eight independent partials
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t ra[32];
+        tmem_ld32(s_addr + c4 * 32, ra);
+        tmem_ld_wait(ra);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(ra[c]));
+      }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      mx *= sl2;  // scale > 0, so the max commutes with the scaling
+      const float m_new = fmaxf(m_run, mx);
+      const bool first = (j == 0);
+      const bool resc = !first && (m_new - m_run > kRescaleThreshold);
+      const float m_ref = (first || resc) ? m_new : m_run;
+      const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+      // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
+      // 64 columns of S_t (chunk c writes columns [16c, 16c+16), which only
+      // chunks <= c have read)
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t ra[32];
+        tmem_ld32(s_addr + c4 * 32, ra);
+        tmem_ld_wait(ra);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(__uint_as_float(ra[2 * e]), sl2, -m_use));
+          const float p1 = ex2(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -m_use));
+          sum8[e & 7] += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c4 * 16, pk);
+      }
+      tmem_st_wait();
+      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      if (!first && __any_sync(0xffffffffu, resc)) {
+        // O_t holds P_0..P_{j-1} V; wait for the last of those MMAs, then rescale
+        if (!(ok = warp_wait(&bars->o_done[t], (j - 1) & 1, ctl, kCode))) break;
+        tc_fence_after();
+        const float corr = resc ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ro[32];
+          tmem_ld32(o_addr + c * 32, ro);
+          tmem_ld_wait(ro);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+          tmem_st32(o_addr + c * 32, ro);
+        }
+        tmem_st_wait();
+        if (resc) l_run *= corr;
+      }
+      if (first || resc) m_run = m_new;
+      l_run += sum;
+      tc_fence_before();
+      warp_arrive(&bars->p_full[t]);
+    }
+    if (ok && nb > 0) ok = warp_wait(&bars->o_done[t], (nb - 1) & 1, ctl, kCode);
+    if (ok && nb > 0) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ro[32];
+        tmem_ld32(o_addr + c * 32, ro);
+        tmem_ld_wait(ro);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+        if (row < s.T) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        }
+      }
+      if (row < s.T) {
+        const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : 0.f;
+        p.LSE[(static_cast<size_t>(b) * s.H + h) * s.T + row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
+  using C = Fwd2Cfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd2_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(ceil_div(ceil_div(p.s.T, kBM), 2), p.s.H, p.s.B);
+  fa_fwd2_bf16_kernel<D><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -360,8 +716,9 @@ cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
-  if (p.s.D == 64) return launch_fwd_d<64>(tm, p, stream);
-  if (p.s.D == 128) return launch_fwd_d<128>(tm, p, stream);
+  const bool two = fwd_two_tiles(p.s);
+  if (p.s.D == 64) return two ? launch_fwd2_d<64>(tm, p, stream) : launch_fwd_d<64>(tm, p, stream);
+  if (p.s.D == 128) return two ? launch_fwd2_d<128>(tm, p, stream) : launch_fwd_d<128>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -96,6 +96,8 @@ struct TensorMaps {
 };
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
+// Whether the bf16 forward runs two query tiles per CTA for this shape.
+bool fwd_two_tiles(const Shape& s);
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 

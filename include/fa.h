@@ -216,6 +216,16 @@ int fa_tile_n(void);
  */
 int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall);
 
+/*
+ * Test hook.  Query tiles per CTA of the bf16 forward: 1 (one 128-row tile),
+ * 2 (two 128-row tiles sharing every K/V block the CTA streams) or 0
+ * (automatic: two whenever the sequence has at least two query tiles).
+ * Both produce the same O and LSE up to fp32 rounding order.  Returns
+ * FA_ERR_INVALID_ARG for any other value.  Affects later calls of this
+ * process only.
+ */
+int fa_debug_fwd_tiles(int tiles);
+
 /* Bit flags of the device error word (which wait gave up). */
 typedef enum {
   FA_DEVERR_FWD_TIMEOUT = 1u << 0,

@@ -97,6 +97,13 @@ def test_no_gpu_means_error_not_fallback(lib):
     assert st in (fb.FA_ERR_CUDA, fb.FA_ERR_UNSUPPORTED)
 
 
+def test_forward_tiles_hook_validates(lib):
+    assert fb.fa_debug_fwd_tiles(3) == fb.FA_ERR_INVALID_ARG
+    assert fb.fa_debug_fwd_tiles(-1) == fb.FA_ERR_INVALID_ARG
+    for t in (1, 2, 0):
+        assert fb.fa_debug_fwd_tiles(t) == fb.FA_OK
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert fb.fa_status_string(code) not in ("", "unknown status")

@@ -114,6 +114,36 @@ def test_small_elementwise(case):
     check_grad(w, "dV", got["dv"], dV)
 
 
+FWD_TILE_CASES = [
+    # dtype, B, H, HKV, T, D, window, causal
+    ("bf16", 2, 4, 2, 300, 64, 0, True),      # 3 query tiles: the last pair has no tile B
+    ("bf16", 1, 2, 2, 129, 128, 0, True),     # tile B holds one row
+    ("bf16", 1, 4, 2, 513, 128, 200, True),   # window: tile A and B ranges differ at both ends
+    ("bf16", 1, 2, 2, 384, 64, 128, True),    # window of one tile
+    ("bf16", 1, 2, 1, 520, 128, 0, False),    # non-causal, ragged
+    ("bf16", 1, 2, 2, 260, 128, 100, False),  # non-causal window
+    ("bf16", 1, 4, 4, 260, 64, 1, True),      # window 1
+    ("bf16", 1, 8, 1, 1024, 128, 0, True),    # GQA 8:1, four pairs
+]
+
+
+@pytest.mark.parametrize("tiles", [1, 2])
+@pytest.mark.parametrize("case", FWD_TILE_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_forward_tiles_per_cta(case, tiles):
+    """Both forward kernels (one or two 128-row query tiles per CTA) against
+    the oracle, element by element."""
+    dtype, B, H, HKV, T, D, window, causal = case
+    w = Workload(103, "tiles", dtype, B, H, HKV, T, D, window, causal, False, "normal")
+    inp = make_inputs(w, seed=2000 + T + D + H + window, with_dO=False)
+    assert fa.fa_debug_fwd_tiles(tiles) == fa.FA_OK
+    try:
+        got = run_gpu(w, inp, bwd=False)
+    finally:
+        fa.fa_debug_fwd_tiles(0)
+    O, LSE = oracle.fwd(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]), w.scale, causal, window)
+    check_fwd(w, got["o"], O, got["lse"], LSE)
+
+
 def test_backward_is_bitwise_reproducible():
     w = Workload(101, "repro", "bf16", 1, 8, 2, 640, 128, 0, True, True, "normal")
     inp = make_inputs(w, seed=7)
