@@ -359,7 +359,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // No S buffer is doubled; the tiles ping-pong instead.  Per streamed block n
 // the MMA queue is  PV_A(n) S_A(n+1) PV_B(n) S_B(n+1), so the softmax of one
 // tile runs while the tensor pipe works on the other's.  S_t(n+1) overwrites
-// the P_t(n) that PV_t(n) reads; the tensor pipe executes in order.
+// the P_t(n) that PV_t(n) reads; the tensor pipe executes in order.  For the
+// same reason a completed S_t(n+1) implies a completed PV_t(n): the softmax
+// may rescale O_t as soon as it sees its scores, and O_t's own barrier is
+// committed only once, after the tile's last PV.
 // A tile skips the streamed blocks outside its own visible range (with a
 // window the first block may be A's only, with causal masking the last is
 // B's only).
@@ -392,7 +395,7 @@ struct Bars2 {
   uint64_t v_empty[4];  // V stage free once the PV MMAs of both tiles completed
   uint64_t s_full[2];   // per tile
   uint64_t p_full[2];   // per tile: one arrival per softmax warp
-  uint64_t o_done[2];   // per tile: its last PV MMA completed
+  uint64_t o_done[2];   // per tile: all its PV MMAs completed (committed once, after the last)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -500,10 +503,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
       int n_s[2] = {0, 0};  // S MMAs issued per tile (s_full phases)
       int n_p[2] = {0, 0};  // PV MMAs issued per tile (p_full phases)
       auto in_tile = [&](int t, int kb) { return t ? (lo_b <= kb && kb <= hi_b) : (lo_a <= kb && kb <= hi_a); };
+      int k_seen = -1;  // last streamed block whose K stage this thread waited for
       auto issue_s = [&](int t, int n) -> bool {  // S_t = Q_t K_n^T
         const int st = n % C::kKStages;
-        if (!wait_bar(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
-        tc_fence_after();
+        if (k_seen < n) {
+          if (!wait_bar(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
+          tc_fence_after();
+          k_seen = n;
+        }
         const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
         const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
 #pragma unroll
@@ -534,7 +541,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             for (int kk = 0; kk < kBN / 16; ++kk)  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
               mma_ts(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
                      (n_p[t] > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&bars->o_done[t]);
+            if (kb == (t ? hi_b : hi_a)) mma_commit(&bars->o_done[t]);  // the tile's last PV
             ++n_p[t];
           }
           if (n + 1 < nblk && in_tile(t, kb + 1)) ok = issue_s(t, n + 1);
@@ -589,12 +596,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t ra[32];
-        tmem_ld32(s_addr + c4 * 32, ra);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(s_addr + c2 * 64, ra);
+        tmem_ld32(s_addr + c2 * 64 + 32, rb);
         tmem_ld_wait(ra);
+        reg_tie(rb);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(ra[c]));
+        for (int c = 0; c < 32; ++c) mx8[c & 7] = fmax3(mx8[c & 7], __uint_as_float(ra[c]), __uint_as_float(rb[c]));
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -606,8 +615,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
       // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
       // 64 columns of S_t (chunk c writes columns [16c, 16c+16), which only
-      // chunks <= c have read)
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // chunks <= c have read).  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
+      // - (m, m) in one instruction; the sum in four packed partials.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t ra[32];
@@ -616,19 +628,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(ra[2 * e]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(ra[2 * e + 1]), sl2, -m_use));
-          sum8[e & 7] += p0 + p1;
+          const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sl2x2, negm2);
+          float x0, x1;
+          f2_unpack(x01, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          sum4[e & 3] = f2_add(sum4[e & 3], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c4 * 16, pk);
       }
       tmem_st_wait();
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      float a0, a1, b0, b1;
+      f2_unpack(f2_add(sum4[0], sum4[1]), a0, a1);
+      f2_unpack(f2_add(sum4[2], sum4[3]), b0, b1);
+      const float sum = (a0 + b0) + (a1 + b1);
       if (!first && __any_sync(0xffffffffu, resc)) {
-        // O_t holds P_0..P_{j-1} V; wait for the last of those MMAs, then rescale
-        if (!(ok = warp_wait(&bars->o_done[t], (j - 1) & 1, ctl, kCode))) break;
-        tc_fence_after();
+        // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order pipe)
         const float corr = resc ? ex2(m_run - m_new) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -647,7 +662,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_before();
       warp_arrive(&bars->p_full[t]);
     }
-    if (ok && nb > 0) ok = warp_wait(&bars->o_done[t], (nb - 1) & 1, ctl, kCode);
+    if (ok && nb > 0) ok = warp_wait(&bars->o_done[t], 0, ctl, kCode);
     if (ok && nb > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
