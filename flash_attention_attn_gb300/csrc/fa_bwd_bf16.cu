@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, g * D + c * 64, kb * BK, b);
       }
     }
-    // LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
+    // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
     // four per lane; read one block ahead so that their latency overlaps the
     // wait for the stage
     float l2[4], dl[4];
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dl[k] = 0.f;
         if (i < s.T) {
           const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
-          l2[k] = p.LSE[idx] * kLog2e;
+          l2[k] = -p.LSE[idx] * kLog2e;
           dl[k] = p.Delta[idx];
         }
       }
@@ -361,14 +361,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           pv[32 + c] = hi[c];
         }
       }
-      const float4* lse4 = reinterpret_cast<const float4*>(rows);
+      const float4* lse4 = reinterpret_cast<const float4*>(rows);  // -LSE*log2e per query
+      const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l = lse4[c4];
-        pv[4 * c4 + 0] = ex2(fmaf(pv[4 * c4 + 0], sl2, -l.x));
-        pv[4 * c4 + 1] = ex2(fmaf(pv[4 * c4 + 1], sl2, -l.y));
-        pv[4 * c4 + 2] = ex2(fmaf(pv[4 * c4 + 2], sl2, -l.z));
-        pv[4 * c4 + 3] = ex2(fmaf(pv[4 * c4 + 3], sl2, -l.w));
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]), sl2x2, f2_pack(l.x, l.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2, f2_pack(l.z, l.w)), x2, x3);
+        pv[4 * c4 + 0] = ex2(x0);
+        pv[4 * c4 + 1] = ex2(x1);
+        pv[4 * c4 + 2] = ex2(x2);
+        pv[4 * c4 + 3] = ex2(x3);
       }
       if (need_mask) {
         const int i0 = qb * BQ + half * 64;
@@ -395,14 +399,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 d = del4[c4];
         const float4 e = del4[8 + c4];
-        dlo[4 * c4 + 0] = pv[4 * c4 + 0] * (dlo[4 * c4 + 0] - d.x);
-        dlo[4 * c4 + 1] = pv[4 * c4 + 1] * (dlo[4 * c4 + 1] - d.y);
-        dlo[4 * c4 + 2] = pv[4 * c4 + 2] * (dlo[4 * c4 + 2] - d.z);
-        dlo[4 * c4 + 3] = pv[4 * c4 + 3] * (dlo[4 * c4 + 3] - d.w);
-        dhi[4 * c4 + 0] = pv[32 + 4 * c4 + 0] * (dhi[4 * c4 + 0] - e.x);
-        dhi[4 * c4 + 1] = pv[32 + 4 * c4 + 1] * (dhi[4 * c4 + 1] - e.y);
-        dhi[4 * c4 + 2] = pv[32 + 4 * c4 + 2] * (dhi[4 * c4 + 2] - e.z);
-        dhi[4 * c4 + 3] = pv[32 + 4 * c4 + 3] * (dhi[4 * c4 + 3] - e.w);
+        // dS = P (dP - Delta), paired
+        f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]),
+                         f2_sub(f2_pack(dlo[4 * c4 + 0], dlo[4 * c4 + 1]), f2_pack(d.x, d.y))),
+                  dlo[4 * c4 + 0], dlo[4 * c4 + 1]);
+        f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
+                         f2_sub(f2_pack(dlo[4 * c4 + 2], dlo[4 * c4 + 3]), f2_pack(d.z, d.w))),
+                  dlo[4 * c4 + 2], dlo[4 * c4 + 3]);
+        f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 0], pv[32 + 4 * c4 + 1]),
+                         f2_sub(f2_pack(dhi[4 * c4 + 0], dhi[4 * c4 + 1]), f2_pack(e.x, e.y))),
+                  dhi[4 * c4 + 0], dhi[4 * c4 + 1]);
+        f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 2], pv[32 + 4 * c4 + 3]),
+                         f2_sub(f2_pack(dhi[4 * c4 + 2], dhi[4 * c4 + 3]), f2_pack(e.z, e.w))),
+                  dhi[4 * c4 + 2], dhi[4 * c4 + 3]);
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -615,10 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         float lo[32], hi[32];
         load_two_cols32(s_addr, s_addr + 32, lo, hi);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pv[c] = ex2(fmaf(lo[c], sl2, -lse2));
-          pv[32 + c] = ex2(fmaf(hi[c], sl2, -lse2));
+        for (int c = 0; c < 32; c += 2) {
+          float x0, x1, y0, y1;
+          f2_unpack(f2_fma(f2_pack(lo[c], lo[c + 1]), sl2x2, nl2), x0, x1);
+          f2_unpack(f2_fma(f2_pack(hi[c], hi[c + 1]), sl2x2, nl2), y0, y1);
+          pv[c] = ex2(x0);
+          pv[c + 1] = ex2(x1);
+          pv[32 + c] = ex2(y0);
+          pv[33 + c] = ex2(y1);
         }
       }
       if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
@@ -633,10 +648,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float lo[32], hi[32];
         load_two_cols32(dp_addr, dp_addr + 32, lo, hi);
         uint32_t pk[32];
+        const uint64_t dl2 = f2_pack(delta, delta);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk[e] = pack_bf16x2(pv[2 * e] * (lo[2 * e] - delta), pv[2 * e + 1] * (lo[2 * e + 1] - delta));
-          pk[16 + e] = pack_bf16x2(pv[32 + 2 * e] * (hi[2 * e] - delta), pv[33 + 2 * e] * (hi[2 * e + 1] - delta));
+        for (int e = 0; e < 16; ++e) {  // dS = P (dP - Delta), paired
+          float a0, a1, b0, b1;
+          f2_unpack(f2_mul(f2_pack(pv[2 * e], pv[2 * e + 1]), f2_sub(f2_pack(lo[2 * e], lo[2 * e + 1]), dl2)), a0, a1);
+          f2_unpack(f2_mul(f2_pack(pv[32 + 2 * e], pv[33 + 2 * e]), f2_sub(f2_pack(hi[2 * e], hi[2 * e + 1]), dl2)), b0,
+                    b1);
+          pk[e] = pack_bf16x2(a0, a1);
+          pk[16 + e] = pack_bf16x2(b0, b1);
         }
         tmem_st32(s_addr, pk);  // dS of keys [64 half, 64 half + 64) -> columns [64 half, 64 half + 32)
       }

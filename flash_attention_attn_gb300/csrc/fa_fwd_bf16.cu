@@ -614,20 +614,22 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const float m_ref = (first || resc) ? m_new : m_run;
       const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
       // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
-      // 64 columns of S_t (chunk c writes columns [16c, 16c+16), which only
-      // chunks <= c have read).  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
+      // 64 columns of S_t (step c writes columns [32c, 32c+32), which only
+      // steps <= c have read).  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
       // - (m, m) in one instruction; the sum in four packed partials.
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm2 = f2_pack(-m_use, -m_use);
       uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t ra[32];
-        tmem_ld32(s_addr + c4 * 32, ra);
-        tmem_ld_wait(ra);
-        uint32_t pk[16];
+      for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per step: two loads in flight
+        uint32_t ra[64];
+        tmem_ld32(s_addr + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
+        tmem_ld32(s_addr + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
+        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
+        reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sl2x2, negm2);
           float x0, x1;
           f2_unpack(x01, x0, x1);
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           sum4[e & 3] = f2_add(sum4[e & 3], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(s_addr + c4 * 16, pk);
+        tmem_st32(s_addr + c2 * 32, pk);
       }
       tmem_st_wait();
       float a0, a1, b0, b1;
