@@ -7,6 +7,7 @@ not been built.
 """
 from ._binding import (  # noqa: F401
     FA_DTYPE_BF16,
+    FA_DTYPE_FP16,
     FA_DTYPE_FP32,
     FA_ERR_CUDA,
     FA_ERR_INVALID_ARG,

@@ -29,6 +29,7 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_WORKSPACE = 5
 FA_DTYPE_BF16 = 0
 FA_DTYPE_FP32 = 1
+FA_DTYPE_FP16 = 2
 FA_OP_FWD = 0
 FA_OP_BWD = 1
 
@@ -193,6 +194,8 @@ def _dtype_code(t) -> int:
         return FA_DTYPE_BF16
     if t.dtype == torch.float32:
         return FA_DTYPE_FP32
+    if t.dtype == torch.float16:
+        return FA_DTYPE_FP16
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 

@@ -31,7 +31,7 @@ int validate_shape(int B, int T, int H, int HKV, int D, float scale, int causal,
   if (H % HKV != 0) return FA_ERR_INVALID_ARG;
   if (window < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale == INFINITY) return FA_ERR_INVALID_ARG;  // also rejects NaN
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   // grid limits (y = heads, z = batch) and 32-bit row indexing inside kernels
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
@@ -83,16 +83,18 @@ int get_encoder() {
   return FA_OK;
 }
 
-// 3-D bf16 view [B][T][heads*D] of a [B,T,heads,D] tensor; boxes of 64
-// elements x box_rows rows x 1 batch, 128-byte swizzle.  Rows past T of a
-// batch read as zeros.
-int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D, int box_rows = 128) {
+// 3-D 16-bit (bf16 or fp16) view [B][T][heads*D] of a [B,T,heads,D] tensor;
+// boxes of 64 elements x 128 rows x 1 batch, 128-byte swizzle.  Rows past T
+// of a batch read as zeros.
+int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D, int dtype) {
   const cuuint64_t inner = static_cast<cuuint64_t>(heads) * D;
   cuuint64_t dims[3] = {inner, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[2] = {inner * 2, inner * 2 * static_cast<cuuint64_t>(T)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType ty =
+      dtype == FA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = g_encode(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
@@ -138,9 +140,9 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
                                          static_cast<const float*>(V), static_cast<float*>(O), LSE, shp, s));
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TensorMaps tm;
-  if ((st = encode_map(&tm.q, Q, B, T, H, head_dim)) != FA_OK) return st;
-  if ((st = encode_map(&tm.k, K, B, T, HKV, head_dim)) != FA_OK) return st;
-  if ((st = encode_map(&tm.v, V, B, T, HKV, head_dim)) != FA_OK) return st;
+  if ((st = encode_map(&tm.q, Q, B, T, H, head_dim, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm.k, K, B, T, HKV, head_dim, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm.v, V, B, T, HKV, head_dim, dtype)) != FA_OK) return st;
   fa::FwdParams p;
   p.s = shp;
   p.O = O;
@@ -149,6 +151,7 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_wait_ns.load();
   p.inject_stall = g_inject_stall.exchange(0);
+  p.f16 = dtype == FA_DTYPE_FP16;
   return status_of(fa::launch_fwd_bf16(tm, p, s));
 }
 
@@ -172,22 +175,19 @@ int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int H, int HKV
   return FA_OK;
 }
 
-int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, const void* dO, const Shape& s) {
+int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, const void* dO, const Shape& s,
+             int dtype) {
   int st;
   if ((st = get_encoder()) != FA_OK) return st;
-  if ((st = encode_map(&tm->q, Q, s.B, s.T, s.H, s.D)) != FA_OK) return st;
-  if ((st = encode_map(&tm->k, K, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
-  if ((st = encode_map(&tm->v, V, s.B, s.T, s.HKV, s.D)) != FA_OK) return st;
-  if ((st = encode_map(&tm->dO, dO, s.B, s.T, s.H, s.D)) != FA_OK) return st;
-  if ((st = encode_map(&tm->q64, Q, s.B, s.T, s.H, s.D, 64)) != FA_OK) return st;
-  if ((st = encode_map(&tm->k64, K, s.B, s.T, s.HKV, s.D, 64)) != FA_OK) return st;
-  if ((st = encode_map(&tm->v64, V, s.B, s.T, s.HKV, s.D, 64)) != FA_OK) return st;
-  if ((st = encode_map(&tm->dO64, dO, s.B, s.T, s.H, s.D, 64)) != FA_OK) return st;
+  if ((st = encode_map(&tm->q, Q, s.B, s.T, s.H, s.D, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm->k, K, s.B, s.T, s.HKV, s.D, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm->v, V, s.B, s.T, s.HKV, s.D, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm->dO, dO, s.B, s.T, s.H, s.D, dtype)) != FA_OK) return st;
   return FA_OK;
 }
 
 fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, void* dQ, void* dK, void* dV,
-                         void* workspace) {
+                         void* workspace, int dtype) {
   fa::BwdParams p;
   p.s = s;
   p.LSE = LSE;
@@ -198,6 +198,7 @@ fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, v
   p.err = static_cast<unsigned int*>(workspace);
   p.scale_log2 = s.scale * 1.4426950408889634f;
   p.timeout_ns = g_wait_ns.load();
+  p.f16 = dtype == FA_DTYPE_FP16;
   return p;
 }
 
@@ -210,7 +211,7 @@ int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HK
   float* delta;
   int st = bwd_prologue(ptrs, 2, B, T, H, HKV, head_dim, 1.f, 1, 0, dtype, workspace, workspace_bytes, &shp, &delta);
   if (st != FA_OK) return st;
-  return status_of(fa::launch_delta(O, dO, delta, shp, dtype == FA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
+  return status_of(fa::launch_delta(O, dO, delta, shp, dtype, static_cast<cudaStream_t>(stream)));
 }
 
 int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
@@ -228,8 +229,8 @@ int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, c
                                               static_cast<const float*>(V), static_cast<const float*>(dO), LSE,
                                               delta, static_cast<float*>(dK), static_cast<float*>(dV), shp, s));
   fa::TensorMaps tm;
-  if ((st = bwd_maps(&tm, Q, K, V, dO, shp)) != FA_OK) return st;
-  return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace), s));
+  if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
+  return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace, dtype), s));
 }
 
 int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
@@ -247,8 +248,8 @@ int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, con
                                             static_cast<const float*>(V), static_cast<const float*>(dO), LSE, delta,
                                             static_cast<float*>(dQ), shp, s));
   fa::TensorMaps tm;
-  if ((st = bwd_maps(&tm, Q, K, V, dO, shp)) != FA_OK) return st;
-  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace), s));
+  if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
+  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype), s));
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,

@@ -77,7 +77,8 @@ __device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float 
 
 // Write `ncols` fp32 TMEM columns of this thread's lane, times `mul`, as bf16
 // to global memory at dst (16-byte aligned, ncols a multiple of 32).
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, __nv_bfloat16* dst,
+template <bool F16>
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, uint16_t* dst,
                                               bool valid) {
   for (int c = 0; c < ncols; c += 32) {
     uint32_t r[32];
@@ -86,7 +87,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e)
-      pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+      pk[e] = pack2<F16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
     if (valid) {
       uint4* d = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
@@ -181,7 +182,7 @@ struct DkdvTiles {
   static constexpr uint32_t kTmDK = 256 + D;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -285,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BQ, false, false);  // K-major x K-major, N = 128
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
+      constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, BQ, false, false);  // K-major x K-major, N = 128
+      constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sK = sbase + C::kOffRes0;
       const uint32_t sV = sbase + C::kOffRes1;
       auto issue_s = [&](int n) -> bool {  // S^T_n = K Q_n^T
@@ -382,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) pk[e] = pack2<F16>(pv[2 * e], pv[2 * e + 1]);
         tmem_st32(s_addr, pk);  // 64 packed values into the first 32 columns of this half
       }
       tmem_st_wait();
@@ -415,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        pk[e] = pack_bf16x2(dlo[2 * e], dlo[2 * e + 1]);
-        pk[16 + e] = pack_bf16x2(dhi[2 * e], dhi[2 * e + 1]);
+        pk[e] = pack2<F16>(dlo[2 * e], dlo[2 * e + 1]);
+        pk[16 + e] = pack2<F16>(dhi[2 * e], dhi[2 * e + 1]);
       }
       tmem_st32(dp_addr, pk);
       tmem_st_wait();
@@ -427,10 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D + half * (D / 2);
-      store_acc_row(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, 1.f,
-                    static_cast<__nv_bfloat16*>(p.dV) + rowoff, j < s.T);
-      store_acc_row(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, s.scale,
-                    static_cast<__nv_bfloat16*>(p.dK) + rowoff, j < s.T);
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, 1.f,
+                    static_cast<uint16_t*>(p.dV) + rowoff, j < s.T);
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, s.scale,
+                    static_cast<uint16_t*>(p.dK) + rowoff, j < s.T);
     }
   }
 
@@ -470,7 +471,7 @@ struct DqTiles {
   static constexpr uint32_t kTmDQ = 384;  // D columns
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -552,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BK, false, false);  // K-major x K-major, N = 128
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, false, true);  // TMEM A x MN-major B, N = D
+      constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, BK, false, false);  // K-major x K-major, N = 128
+      constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sQ = sbase + C::kOffRes0;
       const uint32_t sdO = sbase + C::kOffRes1;
       auto issue_s = [&](int n) -> bool {  // S_n = Q K_n^T into buffer n & 1
@@ -655,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(f2_mul(f2_pack(pv[2 * e], pv[2 * e + 1]), f2_sub(f2_pack(lo[2 * e], lo[2 * e + 1]), dl2)), a0, a1);
           f2_unpack(f2_mul(f2_pack(pv[32 + 2 * e], pv[33 + 2 * e]), f2_sub(f2_pack(hi[2 * e], hi[2 * e + 1]), dl2)), b0,
                     b1);
-          pk[e] = pack_bf16x2(a0, a1);
-          pk[16 + e] = pack_bf16x2(b0, b1);
+          pk[e] = pack2<F16>(a0, a1);
+          pk[16 + e] = pack2<F16>(b0, b1);
         }
         tmem_st32(s_addr, pk);  // dS of keys [64 half, 64 half + 64) -> columns [64 half, 64 half + 32)
       }
@@ -668,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * D + half * (D / 2);
-      store_acc_row(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.scale,
-                    static_cast<__nv_bfloat16*>(p.dQ) + rowoff, i < s.T);
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.scale,
+                    static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T);
     }
   }
 
@@ -682,47 +683,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
   using C = DkdvTiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(ceil_div(p.s.T, 128), p.s.HKV, p.s.B);
-  fa_bwd_dkdv_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
+  fa_bwd_dkdv_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
   using C = DqTiles<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(ceil_div(p.s.T, 128), p.s.H, p.s.B);
-  fa_bwd_dq_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
+  fa_bwd_dq_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  if (p.s.D == 64) return launch_dkdv_d<64>(tm, p, stream);
-  if (p.s.D == 128) return launch_dkdv_d<128>(tm, p, stream);
+  if (p.s.D == 64) return p.f16 ? launch_dkdv_d<64, true>(tm, p, stream) : launch_dkdv_d<64, false>(tm, p, stream);
+  if (p.s.D == 128) return p.f16 ? launch_dkdv_d<128, true>(tm, p, stream) : launch_dkdv_d<128, false>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  if (p.s.D == 64) return launch_dq_d<64>(tm, p, stream);
-  if (p.s.D == 128) return launch_dq_d<128>(tm, p, stream);
+  if (p.s.D == 64) return p.f16 ? launch_dq_d<64, true>(tm, p, stream) : launch_dq_d<64, false>(tm, p, stream);
+  if (p.s.D == 128) return p.f16 ? launch_dq_d<128, true>(tm, p, stream) : launch_dq_d<128, false>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -1,4 +1,5 @@
 // fa_delta.cu -- backward preprocess: Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]
+// (bf16, fp16 or fp32 elements, fp32 accumulation)
 // (the identity rowsum(dO * O) = rowsum(dP * P) named in the forge page,
 // flash_attention.metal, backward section; the Graphcore page computes the
 // same D before its block loops).
@@ -9,6 +10,7 @@
 // 32-byte sectors), every thread issues all of its loads before reducing, and
 // the 64 results leave as one contiguous 256-byte store.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "fa_internal.h"
 
@@ -26,6 +28,20 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const __n
   for (int k = 0; k < 4; ++k) {
     const float2 fx = __bfloat1622float2(x[k]);
     const float2 fy = __bfloat1622float2(y[k]);
+    acc = fmaf(fx.x, fy.x, acc);
+    acc = fmaf(fx.y, fy.y, acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const __half*) {
+  const __half2* x = reinterpret_cast<const __half2*>(&a);
+  const __half2* y = reinterpret_cast<const __half2*>(&b);
+  float acc = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 fx = __half22float2(x[k]);
+    const float2 fy = __half22float2(y[k]);
     acc = fmaf(fx.x, fy.x, acc);
     acc = fmaf(fx.y, fy.y, acc);
   }
@@ -90,12 +106,15 @@ cudaError_t launch(const void* O, const void* dO, float* Delta, const Shape& s, 
 
 }  // namespace
 
-cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, bool bf16,
+cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, int elem,
                          cudaStream_t stream) {
-  if (bf16) {
+  if (elem == 0) {  // bf16
     if (s.D == 64) return launch<__nv_bfloat16, 64>(O, dO, Delta, s, stream);
     if (s.D == 128) return launch<__nv_bfloat16, 128>(O, dO, Delta, s, stream);
-  } else {
+  } else if (elem == 2) {  // fp16
+    if (s.D == 64) return launch<__half, 64>(O, dO, Delta, s, stream);
+    if (s.D == 128) return launch<__half, 128>(O, dO, Delta, s, stream);
+  } else {  // fp32
     if (s.D == 64) return launch<float, 64>(O, dO, Delta, s, stream);
     if (s.D == 128) return launch<float, 128>(O, dO, Delta, s, stream);
   }

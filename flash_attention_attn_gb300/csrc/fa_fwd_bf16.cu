@@ -77,7 +77,7 @@ __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
                  "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -169,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 5) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_f32acc<F16>(128, D, false, true);
       bool ok = wait_bar(&bars->q_tmem, 0, ctl, kCode);
       for (int n = 0; ok && n <= nblk; ++n) {
         if (n < nblk) {
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = ex2(fmaf(sv[q4 * 32 + 2 * e], sl2, -m_use));
           const float p1 = ex2(fmaf(sv[q4 * 32 + 2 * e + 1], sl2, -m_use));
           sum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          pk[e] = pack2<F16>(p0, p1);
         }
         tmem_st16(s_addr + q4 * 16, pk);
       }
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const uint32_t o_addr = tmem + lane_addr + C::kTmO;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ro[32];
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+          pk[e] = pack2<F16>(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
         if (row < s.T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -401,7 +401,7 @@ struct Bars2 {
   int abort;
 };
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads2, 1)
     fa_fwd2_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // Q x K^T, both K-major
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);     // P (TMEM) x V (MN-major)
+      constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, 128, false, false);  // Q x K^T, both K-major
+      constexpr uint32_t idesc_o = idesc_f32acc<F16>(128, D, false, true);     // P (TMEM) x V (MN-major)
       int n_s[2] = {0, 0};  // S MMAs issued per tile (s_full phases)
       int n_p[2] = {0, 0};  // PV MMAs issued per tile (p_full phases)
       auto in_tile = [&](int t, int kb) { return t ? (lo_b <= kb && kb <= hi_b) : (lo_a <= kb && kb <= hi_a); };
@@ -635,7 +635,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           f2_unpack(x01, x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
           sum4[e & 3] = f2_add(sum4[e & 3], f2_pack(p0, p1));
-          pk[e] = pack_bf16x2(p0, p1);
+          pk[e] = pack2<F16>(p0, p1);
         }
         tmem_st32(s_addr + c2 * 32, pk);
       }
@@ -668,7 +668,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (ok && nb > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ro[32];
@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+          pk[e] = pack2<F16>(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
         if (row < s.T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -700,43 +700,48 @@ __global__ void __launch_bounds__(kThreads2, 1)
   }
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   using C = Fwd2Cfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd2_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd2_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(ceil_div(ceil_div(p.s.T, kBM), 2), p.s.H, p.s.B);
-  fa_fwd2_bf16_kernel<D><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
+  fa_fwd2_bf16_kernel<D, F16><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F16>
 cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid(ceil_div(p.s.T, kBM), p.s.H, p.s.B);
-  fa_fwd_bf16_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
+  fa_fwd_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
+template <bool F16>
+cudaError_t launch_fwd_t(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   const bool two = fwd_two_tiles(p.s);
-  if (p.s.D == 64) return two ? launch_fwd2_d<64>(tm, p, stream) : launch_fwd_d<64>(tm, p, stream);
-  if (p.s.D == 128) return two ? launch_fwd2_d<128>(tm, p, stream) : launch_fwd_d<128>(tm, p, stream);
+  if (p.s.D == 64) return two ? launch_fwd2_d<64, F16>(tm, p, stream) : launch_fwd_d<64, F16>(tm, p, stream);
+  if (p.s.D == 128) return two ? launch_fwd2_d<128, F16>(tm, p, stream) : launch_fwd_d<128, F16>(tm, p, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
+  return p.f16 ? launch_fwd_t<true>(tm, p, stream) : launch_fwd_t<false>(tm, p, stream);
 }
 
 }  // namespace fa

@@ -74,6 +74,7 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e)
   uint64_t timeout_ns;
   int inject_stall;
+  int f16;            // elements are fp16 (else bf16)
 };
 
 struct BwdParams {
@@ -86,13 +87,13 @@ struct BwdParams {
   unsigned int* err;
   float scale_log2;
   uint64_t timeout_ns;
+  int f16;            // elements are fp16 (else bf16)
 };
 
 // 3-D views [B][T][heads*D] with boxes of 64 elements x R rows x 1 batch:
 // R = 128 for the plain maps, R = 64 for the *64 maps.
 struct TensorMaps {
   CUtensorMap q, k, v, dO;
-  CUtensorMap q64, k64, v64, dO64;
 };
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
@@ -104,7 +105,8 @@ cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStr
 // ---------------------------------------------------------- shared kernels
 
 // Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d], fp32 accumulation.
-cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, bool bf16,
+// elem: 0 bf16, 1 fp32, 2 fp16 (the fa_dtype values)
+cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, int elem,
                          cudaStream_t stream);
 
 // ----------------------------------------------------------- fp32 kernels

@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace fa {
@@ -158,14 +159,19 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Instruction descriptor of a kind::f16 MMA with bf16 A and B and an fp32
-// accumulator.  Fields (bit ranges): [4,6) D format (1 = f32), [7,10) A
-// format (1 = bf16), [10,13) B format (1 = bf16), 15 A major-ness, 16 B
-// major-ness (0 = K-major, 1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+// Instruction descriptor of a kind::f16 MMA with 16-bit A and B of one type
+// (bf16, or fp16 when F16) and an fp32 accumulator.  Fields (bit ranges):
+// [4,6) D format (1 = f32), [7,10) A format and [10,13) B format (0 = f16,
+// 1 = bf16), 15 A major-ness, 16 B major-ness (0 = K-major, 1 = MN-major),
+// [17,23) N >> 3, [24,29) M >> 4.
+template <bool F16>
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((F16 ? 0u : 1u) << 7) | ((F16 ? 0u : 1u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_f32acc<false>(M, N, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.  Fields: [0,14) start
@@ -349,6 +355,18 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats to a packed fp16x2 (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The 16-bit pair of the kernel's element type.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 }  // namespace ptx

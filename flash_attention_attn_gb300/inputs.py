@@ -6,7 +6,7 @@ oracle) receive tensors made here, so they see bit-identical inputs.
 
 Recipe (one CPU ``torch.Generator`` per workload, seed = the workload id):
 draw fp32 N(0, 1) in the order Q, K, V, dO, then shape them per workload and
-round to the compute dtype (bf16 round-to-nearest-even, or keep fp32).
+round to the compute dtype (bf16 or fp16 round-to-nearest-even, or keep fp32).
 
 * ``rms_qk``: every Q and K head vector is RMS-normalised,
   x / sqrt(mean(x^2) + eps) with eps = 1.1920928955078125e-7, the QK-norm
@@ -31,7 +31,7 @@ class Workload:
 
     wid: int
     name: str
-    dtype: str  # "bf16" or "fp32"
+    dtype: str  # "bf16", "fp16" or "fp32"
     B: int
     H: int
     HKV: int
@@ -62,7 +62,7 @@ WORKLOADS: dict[int, Workload] = {
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "fp32": torch.float32}[name]
+    return {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[name]
 
 
 def make_inputs(w: Workload, seed: int | None = None, with_dO: bool = True) -> dict[str, torch.Tensor]:

@@ -54,8 +54,9 @@
  * kernel set the error word and exit, which fa_check_status() reports as
  * FA_ERR_TIMEOUT.
  *
- * Supported: dtype FA_DTYPE_BF16 (tcgen05 tensor-core kernels, fp32
- * accumulation) or FA_DTYPE_FP32 (fp32 CUDA-core kernels); head_dim 64 or
+ * Supported: dtype FA_DTYPE_BF16 or FA_DTYPE_FP16 (tcgen05 tensor-core
+ * kernels, fp32 accumulation; P and dS are rounded to the input type before
+ * their MMAs) or FA_DTYPE_FP32 (fp32 CUDA-core kernels); head_dim 64 or
  * 128; any B, T, H, HKV >= 1 with H % HKV == 0; scale > 0 and finite;
  * window >= 0; 16-byte aligned tensor pointers.  No fallback path exists: an
  * unsupported shape is an error.
@@ -78,7 +79,7 @@ typedef enum {
   FA_ERR_WORKSPACE = 5     /* workspace missing, too small or misaligned */
 } fa_status;
 
-typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1 } fa_dtype;
+typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1, FA_DTYPE_FP16 = 2 } fa_dtype;
 
 typedef enum { FA_OP_FWD = 0, FA_OP_BWD = 1 } fa_op;
 

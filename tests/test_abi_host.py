@@ -48,6 +48,9 @@ def test_workspace_sizes(lib):
     assert bwd >= 256 + 4 * 2 * 8 * 1000 and bwd % 256 == 0
     assert fb.fa_workspace_size(fb.FA_OP_BWD, 1, 128, 3, 2, 64, fb.FA_DTYPE_BF16) == 0  # H % HKV
     assert fb.fa_workspace_size(7, 1, 128, 2, 2, 64, fb.FA_DTYPE_BF16) == 0
+    # fp16 runs the same kernels with the same workspace
+    assert fb.fa_workspace_size(fb.FA_OP_BWD, 2, 1000, 8, 2, 128, fb.FA_DTYPE_FP16) == bwd
+    assert fb.fa_workspace_size(fb.FA_OP_BWD, 2, 1000, 8, 2, 128, 3) == 0
 
 
 FAKE = 0x10000  # aligned, never dereferenced: validation fails first
@@ -71,6 +74,8 @@ def call_fwd(B=1, T=128, H=2, HKV=2, D=64, scale=0.125, causal=1, window=0, dtyp
     (dict(causal=2), fb.FA_ERR_INVALID_ARG),
     (dict(D=96), fb.FA_ERR_UNSUPPORTED),
     (dict(dtype=5), fb.FA_ERR_UNSUPPORTED),
+    (dict(dtype=3), fb.FA_ERR_UNSUPPORTED),
+    (dict(dtype=fb.FA_DTYPE_FP16, D=96), fb.FA_ERR_UNSUPPORTED),
     (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE, FAKE + 8, FAKE, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
     (dict(ws=0), fb.FA_ERR_WORKSPACE),

@@ -8,7 +8,7 @@ identities that hold at any size.
 
 Tolerances (fixed for this method):
   fp32  : max |err| <= 1e-4 on O, dQ, dK, dV
-  bf16  : max |err| <= 2e-2 on O; relative Frobenius <= 2e-2 on dQ, dK, dV
+  bf16, fp16 : max |err| <= 2e-2 on O; relative Frobenius <= 2e-2 on dQ, dK, dV
   LSE   : max |err| <= 1e-3
 """
 from __future__ import annotations
@@ -23,7 +23,7 @@ from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, as_f64, make_
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"fp32": dict(o=1e-4, grad_abs=1e-4), "bf16": dict(o=2e-2, grad_rel=2e-2)}
+TOL = {"fp32": dict(o=1e-4, grad_abs=1e-4), "bf16": dict(o=2e-2, grad_rel=2e-2), "fp16": dict(o=2e-2, grad_rel=2e-2)}
 LSE_TOL = 1e-3
 
 
@@ -74,7 +74,7 @@ def check_grad(w, name, got, ref):
         assert err <= 1e-4, f"{name} (exactly zero) max-abs {err:.3e}"
     else:
         err = rel_fro(got, ref)
-        assert err <= TOL["bf16"]["grad_rel"], f"{name} rel-Frobenius {err:.3e}"
+        assert err <= TOL[w.dtype]["grad_rel"], f"{name} rel-Frobenius {err:.3e}"
 
 
 # ------------------------------------------------------ small, element-wise
@@ -96,6 +96,12 @@ SMALL = [
     ("bf16", 1, 2, 2, 129, 128, 0, True),
     ("bf16", 1, 4, 4, 260, 64, 1, True),      # window 1: O = V
     ("bf16", 1, 2, 1, 200, 128, 4096, True),  # window past T
+    # fp16 elements through the same tensor-core kernels
+    ("fp16", 2, 4, 2, 300, 64, 0, True),
+    ("fp16", 1, 8, 2, 513, 128, 0, True),
+    ("fp16", 1, 4, 2, 513, 128, 200, True),
+    ("fp16", 1, 2, 1, 130, 128, 0, False),
+    ("fp16", 1, 2, 2, 1, 64, 0, True),
 ]
 
 
@@ -124,6 +130,8 @@ FWD_TILE_CASES = [
     ("bf16", 1, 2, 2, 260, 128, 100, False),  # non-causal window
     ("bf16", 1, 4, 4, 260, 64, 1, True),      # window 1
     ("bf16", 1, 8, 1, 1024, 128, 0, True),    # GQA 8:1, four pairs
+    ("fp16", 1, 4, 2, 513, 128, 200, True),
+    ("fp16", 2, 4, 2, 300, 64, 0, True),
 ]
 
 
