@@ -32,7 +32,13 @@ int validate_shape(int B, int T, int H, int HKV, int D, float scale, int causal,
   if (window < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (!(scale > 0.f) || scale == INFINITY) return FA_ERR_INVALID_ARG;  // also rejects NaN
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_FP32) {
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  } else if (D < 16 || D > 128 || D % 8 != 0) {
+    // 16-bit tensor-core path: the kernels run at 64 or 128 and read zeros
+    // past D (TMA fill); D % 8 keeps every row 16-byte aligned
+    return FA_ERR_UNSUPPORTED;
+  }
   // grid limits (y = heads, z = batch) and 32-bit row indexing inside kernels
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * T * H * D >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
@@ -83,18 +89,19 @@ int get_encoder() {
   return FA_OK;
 }
 
-// 3-D 16-bit (bf16 or fp16) view [B][T][heads*D] of a [B,T,heads,D] tensor;
-// boxes of 64 elements x 128 rows x 1 batch, 128-byte swizzle.  Rows past T
-// of a batch read as zeros.
+// 4-D 16-bit (bf16 or fp16) view [B][T][heads][D] of a [B,T,heads,D] tensor;
+// boxes of 64 elements x 1 head x 128 rows x 1 batch, 128-byte swizzle.
+// Elements past D (head dims below 64 or 128) and rows past T read as zeros.
 int encode_map(CUtensorMap* map, const void* base, int B, int T, int heads, int D, int dtype) {
-  const cuuint64_t inner = static_cast<cuuint64_t>(heads) * D;
-  cuuint64_t dims[3] = {inner, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[2] = {inner * 2, inner * 2 * static_cast<cuuint64_t>(T)};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint64_t row = static_cast<cuuint64_t>(heads) * D * 2;  // bytes per position
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, row, row * static_cast<cuuint64_t>(T)};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty =
       dtype == FA_DTYPE_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUresult r = g_encode(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, ty, 4, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;

@@ -77,8 +77,10 @@ __device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float 
 
 // Write `ncols` fp32 TMEM columns of this thread's lane, times `mul`, as bf16
 // to global memory at dst (16-byte aligned, ncols a multiple of 32).
+// ncols accumulator columns of this thread's lane, scaled, as 16-bit values;
+// only the first nvalid columns are stored (a head dim below the kernel's).
 template <bool F16>
-__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float mul, uint16_t* dst,
+__device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, int nvalid, float mul, uint16_t* dst,
                                               bool valid) {
   for (int c = 0; c < ncols; c += 32) {
     uint32_t r[32];
@@ -91,7 +93,8 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, float m
     if (valid) {
       uint4* d = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-      for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      for (int v = 0; v < 4; ++v)
+        if (c + v * 8 < nvalid) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     }
   }
 }
@@ -229,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmdO);
       mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, g * D + c * 64, kb * BK, b);
-        tma_load_3d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, g * D + c * 64, kb * BK, b);
+        tma_load_4d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, g, kb * BK, b);
+        tma_load_4d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, g, kb * BK, b);
       }
     }
     // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
@@ -262,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTile);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, h * D + c * 64,
+          tma_load_4d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
                       qb * BQ, b);
-          tma_load_3d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, h * D + c * 64,
+          tma_load_4d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
                       qb * BQ, b);
         }
       }
@@ -427,11 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
-      const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D + half * (D / 2);
-      store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, 1.f,
-                    static_cast<uint16_t*>(p.dV) + rowoff, j < s.T);
-      store_acc_row<F16>(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, s.scale,
-                    static_cast<uint16_t*>(p.dK) + rowoff, j < s.T);
+      const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * s.D + half * (D / 2);
+      const int nvalid = s.D - half * (D / 2);  // columns of this half inside the head dim
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, nvalid, 1.f,
+                         static_cast<uint16_t*>(p.dV) + rowoff, j < s.T);
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, nvalid, s.scale,
+                         static_cast<uint16_t*>(p.dK) + rowoff, j < s.T);
     }
   }
 
@@ -518,8 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmdO);
       mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, h * D + c * 64, qb * BQ, b);
-        tma_load_3d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, h * D + c * 64, qb * BQ, b);
+        tma_load_4d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
+        tma_load_4d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
       }
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= C::kKStages && !wait_bar(&bars->x_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->x_full[st], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmK, &bars->x_full[st], smem + C::kOffK + st * C::kTile + c * C::kChunk, g * D + c * 64,
+          tma_load_4d(&tmK, &bars->x_full[st], smem + C::kOffK + st * C::kTile + c * C::kChunk, c * 64, g,
                       (kb_lo + n) * BK, b);
         issued = n + 1;
       }
@@ -543,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= C::kVStages && !wait_bar(&bars->v_empty[st], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmV, &bars->v_full[st], smem + C::kOffV + st * C::kTile + c * C::kChunk, g * D + c * 64,
+          tma_load_4d(&tmV, &bars->v_full[st], smem + C::kOffV + st * C::kTile + c * C::kChunk, c * 64, g,
                       (kb_lo + n) * BK, b);
         issued = n + 1;
       }
@@ -668,9 +672,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
-      const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * D + half * (D / 2);
-      store_acc_row<F16>(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.scale,
-                    static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T);
+      const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * s.D + half * (D / 2);
+      store_acc_row<F16>(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.D - half * (D / 2), s.scale,
+                         static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T);
     }
   }
 
@@ -716,14 +720,14 @@ cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t s
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  if (p.s.D == 64) return p.f16 ? launch_dkdv_d<64, true>(tm, p, stream) : launch_dkdv_d<64, false>(tm, p, stream);
-  if (p.s.D == 128) return p.f16 ? launch_dkdv_d<128, true>(tm, p, stream) : launch_dkdv_d<128, false>(tm, p, stream);
+  if (p.s.D <= 64) return p.f16 ? launch_dkdv_d<64, true>(tm, p, stream) : launch_dkdv_d<64, false>(tm, p, stream);
+  if (p.s.D <= 128) return p.f16 ? launch_dkdv_d<128, true>(tm, p, stream) : launch_dkdv_d<128, false>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
-  if (p.s.D == 64) return p.f16 ? launch_dq_d<64, true>(tm, p, stream) : launch_dq_d<64, false>(tm, p, stream);
-  if (p.s.D == 128) return p.f16 ? launch_dq_d<128, true>(tm, p, stream) : launch_dq_d<128, false>(tm, p, stream);
+  if (p.s.D <= 64) return p.f16 ? launch_dq_d<64, true>(tm, p, stream) : launch_dq_d<64, false>(tm, p, stream);
+  if (p.s.D <= 128) return p.f16 ? launch_dq_d<128, true>(tm, p, stream) : launch_dq_d<128, false>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -54,9 +54,12 @@ __device__ __forceinline__ float dot16(const uint4& a, const uint4& b, const flo
   return fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w)));
 }
 
-template <typename T, int D>
+// D: 64 or 128 lanes' worth of row; Dact <= D elements of it are real (the
+// rest read as zeros).  EXACT: Dact == D, known at compile time.
+template <typename T, int D, bool EXACT>
 __global__ void __launch_bounds__(kThreads) fa_bwd_delta_kernel(const T* __restrict__ O, const T* __restrict__ dO,
-                                                                float* __restrict__ Delta, int Tlen, int H) {
+                                                                float* __restrict__ Delta, int Tlen, int H, int Dact) {
+  if (EXACT) Dact = D;
   constexpr int kVec = 16 / sizeof(T);               // elements per 16-byte load
   constexpr int kLanes = D / kVec;                   // lanes per row (8, 16 or 32)
   constexpr int kRowsPerPass = kThreads / kLanes;
@@ -73,8 +76,8 @@ __global__ void __launch_bounds__(kThreads) fa_bwd_delta_kernel(const T* __restr
 #pragma unroll
   for (int ps = 0; ps < kPasses; ++ps) {
     const int t = t0 + ps * kRowsPerPass + r0;
-    if (t < Tlen) {
-      const size_t off = ((static_cast<size_t>(b) * Tlen + t) * H + h) * D + sub * kVec;
+    if (t < Tlen && sub * kVec < Dact) {
+      const size_t off = ((static_cast<size_t>(b) * Tlen + t) * H + h) * Dact + sub * kVec;
       xo[ps] = __ldg(reinterpret_cast<const uint4*>(O + off));
       xd[ps] = __ldg(reinterpret_cast<const uint4*>(dO + off));
     } else {
@@ -99,8 +102,12 @@ __global__ void __launch_bounds__(kThreads) fa_bwd_delta_kernel(const T* __restr
 template <typename T, int D>
 cudaError_t launch(const void* O, const void* dO, float* Delta, const Shape& s, cudaStream_t stream) {
   dim3 grid(ceil_div(s.T, kRowsPerCta), s.H, s.B);
-  fa_bwd_delta_kernel<T, D><<<grid, kThreads, 0, stream>>>(static_cast<const T*>(O), static_cast<const T*>(dO),
-                                                          Delta, s.T, s.H);
+  if (s.D == D)
+    fa_bwd_delta_kernel<T, D, true><<<grid, kThreads, 0, stream>>>(static_cast<const T*>(O),
+                                                                   static_cast<const T*>(dO), Delta, s.T, s.H, D);
+  else
+    fa_bwd_delta_kernel<T, D, false><<<grid, kThreads, 0, stream>>>(static_cast<const T*>(O),
+                                                                    static_cast<const T*>(dO), Delta, s.T, s.H, s.D);
   return cudaGetLastError();
 }
 
@@ -109,11 +116,11 @@ cudaError_t launch(const void* O, const void* dO, float* Delta, const Shape& s, 
 cudaError_t launch_delta(const void* O, const void* dO, float* Delta, const Shape& s, int elem,
                          cudaStream_t stream) {
   if (elem == 0) {  // bf16
-    if (s.D == 64) return launch<__nv_bfloat16, 64>(O, dO, Delta, s, stream);
-    if (s.D == 128) return launch<__nv_bfloat16, 128>(O, dO, Delta, s, stream);
+    if (s.D <= 64) return launch<__nv_bfloat16, 64>(O, dO, Delta, s, stream);
+    if (s.D <= 128) return launch<__nv_bfloat16, 128>(O, dO, Delta, s, stream);
   } else if (elem == 2) {  // fp16
-    if (s.D == 64) return launch<__half, 64>(O, dO, Delta, s, stream);
-    if (s.D == 128) return launch<__half, 128>(O, dO, Delta, s, stream);
+    if (s.D <= 64) return launch<__half, 64>(O, dO, Delta, s, stream);
+    if (s.D <= 128) return launch<__half, 128>(O, dO, Delta, s, stream);
   } else {  // fp32
     if (s.D == 64) return launch<float, 64>(O, dO, Delta, s, stream);
     if (s.D == 128) return launch<float, 128>(O, dO, Delta, s, stream);

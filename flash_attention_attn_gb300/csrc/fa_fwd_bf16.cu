@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(&tmQ, &bars->q_full, smem + C::kOffQ + c * C::kChunkBytes, h * D + c * 64, qb * kBM, b);
+        tma_load_4d(&tmQ, &bars->q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, h, qb * kBM, b);
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
         const int st = n % C::kStages;
@@ -147,14 +147,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n >= C::kStages && !wait_bar(&bars->k_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+          tma_load_4d(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
         if (n >= C::kStages && !wait_bar(&bars->v_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) {
           drain_bar(&bars->k_full[st], (n / C::kStages) & 1, p.timeout_ns);
           break;
         }
         mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, g * D + c * 64, kb * kBN, b);
+          tma_load_4d(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
         issued = n + 1;
       }
       if (bars->abort) {
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const uint32_t o_addr = tmem + lane_addr + C::kTmO;
-      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * s.D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ro[32];
@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row < s.T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)  // columns past a head dim below D are not stored
+            if (c * 32 + v * 8 < s.D) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (row < s.T) {
@@ -467,7 +468,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
       for (int t = 0; t < (has_b ? 2 : 1); ++t)
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, h * D + c * 64,
+          tma_load_4d(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64, h,
                       (2 * pair + t) * kBM, b);
       int issued_k = 0, issued_v = 0;
       for (int n = 0; n < nblk; ++n) {
@@ -475,15 +476,15 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (n >= C::kKStages && !wait_bar(&bars->k_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
-                      g * D + c * 64, (lo + n) * kBN, b);
+          tma_load_4d(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, g, (lo + n) * kBN, b);
         issued_k = n + 1;
         const int sv = n % C::kVStages;
         if (n >= C::kVStages && !wait_bar(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
         mbar_arrive_expect_tx(&bars->v_full[sv], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
-                      g * D + c * 64, (lo + n) * kBN, b);
+          tma_load_4d(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, g, (lo + n) * kBN, b);
         issued_v = n + 1;
       }
       if (bars->abort) {
@@ -668,7 +669,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     if (ok && nb > 0) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * D;
+      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * s.D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ro[32];
@@ -681,7 +682,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (row < s.T) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          for (int v = 0; v < 4; ++v)  // columns past a head dim below D are not stored
+            if (c * 32 + v * 8 < s.D) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
       if (row < s.T) {
@@ -735,8 +737,9 @@ cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t 
 template <bool F16>
 cudaError_t launch_fwd_t(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   const bool two = fwd_two_tiles(p.s);
-  if (p.s.D == 64) return two ? launch_fwd2_d<64, F16>(tm, p, stream) : launch_fwd_d<64, F16>(tm, p, stream);
-  if (p.s.D == 128) return two ? launch_fwd2_d<128, F16>(tm, p, stream) : launch_fwd_d<128, F16>(tm, p, stream);
+  // head dims up to 64 run the 64-wide kernels, up to 128 the 128-wide ones
+  if (p.s.D <= 64) return two ? launch_fwd2_d<64, F16>(tm, p, stream) : launch_fwd_d<64, F16>(tm, p, stream);
+  if (p.s.D <= 128) return two ? launch_fwd2_d<128, F16>(tm, p, stream) : launch_fwd_d<128, F16>(tm, p, stream);
   return cudaErrorInvalidValue;
 }
 

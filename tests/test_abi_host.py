@@ -72,10 +72,13 @@ def call_fwd(B=1, T=128, H=2, HKV=2, D=64, scale=0.125, causal=1, window=0, dtyp
     (dict(scale=float("nan")), fb.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fb.FA_ERR_INVALID_ARG),
     (dict(causal=2), fb.FA_ERR_INVALID_ARG),
-    (dict(D=96), fb.FA_ERR_UNSUPPORTED),
+    (dict(D=100), fb.FA_ERR_UNSUPPORTED),   # head dim not a multiple of 8
+    (dict(D=136), fb.FA_ERR_UNSUPPORTED),   # above 128
+    (dict(D=8), fb.FA_ERR_UNSUPPORTED),     # below 16
+    (dict(D=96, dtype=fb.FA_DTYPE_FP32), fb.FA_ERR_UNSUPPORTED),  # fp32 kernels: 64 or 128 only
     (dict(dtype=5), fb.FA_ERR_UNSUPPORTED),
     (dict(dtype=3), fb.FA_ERR_UNSUPPORTED),
-    (dict(dtype=fb.FA_DTYPE_FP16, D=96), fb.FA_ERR_UNSUPPORTED),
+    (dict(dtype=fb.FA_DTYPE_FP16, D=100), fb.FA_ERR_UNSUPPORTED),
     (dict(ptrs=[FAKE, 0, FAKE, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
     (dict(ptrs=[FAKE, FAKE + 8, FAKE, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
     (dict(ws=0), fb.FA_ERR_WORKSPACE),

@@ -96,6 +96,15 @@ SMALL = [
     ("bf16", 1, 2, 2, 129, 128, 0, True),
     ("bf16", 1, 4, 4, 260, 64, 1, True),      # window 1: O = V
     ("bf16", 1, 2, 1, 200, 128, 4096, True),  # window past T
+    # head dims other than 64 and 128 (the kernels run at 64 or 128 and read
+    # zeros past D)
+    ("bf16", 1, 4, 2, 300, 16, 0, True),
+    ("bf16", 2, 2, 1, 200, 32, 0, True),
+    ("bf16", 1, 4, 2, 260, 48, 100, True),
+    ("bf16", 1, 4, 4, 300, 80, 0, True),
+    ("bf16", 1, 8, 2, 513, 96, 0, True),
+    ("bf16", 1, 2, 1, 130, 96, 0, False),
+    ("fp16", 1, 4, 2, 300, 96, 0, True),
     # fp16 elements through the same tensor-core kernels
     ("fp16", 2, 4, 2, 300, 64, 0, True),
     ("fp16", 1, 8, 2, 513, 128, 0, True),
@@ -132,6 +141,8 @@ FWD_TILE_CASES = [
     ("bf16", 1, 8, 1, 1024, 128, 0, True),    # GQA 8:1, four pairs
     ("fp16", 1, 4, 2, 513, 128, 200, True),
     ("fp16", 2, 4, 2, 300, 64, 0, True),
+    ("bf16", 1, 4, 2, 513, 96, 0, True),
+    ("bf16", 1, 2, 2, 300, 48, 64, True),
 ]
 
 
