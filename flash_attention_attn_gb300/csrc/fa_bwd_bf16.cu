@@ -147,7 +147,7 @@ __device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint32_t a_smem, int a
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t ao = (kk >> 2) * a_chunk + (kk & 3) * 32;
     const uint32_t bo = (kk >> 2) * b_chunk + (kk & 3) * 32;
-    mma_ss(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, kk > 0 ? 1u : 0u);
+    mma_ss_e(d_tmem, a0 + (ao >> 4), b0 + (bo >> 4), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -288,51 +288,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, BQ, false, false);  // K-major x K-major, N = 128
       constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sK = sbase + C::kOffRes0;
       const uint32_t sV = sbase + C::kOffRes1;
       auto issue_s = [&](int n) -> bool {  // S^T_n = K Q_n^T
         const int st = n % C::kStages;
-        if (!wait_bar(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
+        if (!warp_wait(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
         issue_kk<D>(tmem + C::kTmS, sK, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk, idesc_s);
-        mma_commit(&bars->s_full[0]);
+        mma_commit_e(&bars->s_full[0]);
         return true;
       };
       auto issue_dp = [&](int n) {  // dP^T_n = V dO_n^T (stage already waited for by issue_s)
         issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + (n % C::kStages) * C::kTile, C::kChunk,
                     idesc_s);
-        mma_commit(&bars->dp_full[0]);
+        mma_commit_e(&bars->dp_full[0]);
       };
       // acc (+)= A[TMEM, 128 packed query rows] x B[128 query rows][D] (MN-major)
       auto issue_acc128 = [&](uint32_t acc, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
         const uint64_t b0 = sdesc_sw128(b_smem, C::kChunk, 1024);
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
-          mma_ts(acc, a_tmem + packed_slice_col128(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc,
+          mma_ts_e(acc, a_tmem + packed_slice_col128(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc,
                  (accumulate || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
+      bool ok = warp_wait(&bars->res_full, 0, ctl, kCode);
       if (ok && niter > 0) {
         ok = issue_s(0);
         if (ok) issue_dp(0);
       }
       for (int n = 0; ok && n < niter; ++n) {
         const int st = n % C::kStages;
-        if (!(ok = wait_bar(&bars->p_full[0], n & 1, ctl, kCode))) break;
+        if (!(ok = warp_wait(&bars->p_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
         issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + st * C::kTile, n > 0);  // dV += P^T dO
         if (n + 1 < niter && !(ok = issue_s(n + 1))) break;  // P^T_n is read by the dV MMAs queued above
-        if (!(ok = wait_bar(&bars->ds_full[0], n & 1, ctl, kCode))) break;
+        if (!(ok = warp_wait(&bars->ds_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
         issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + st * C::kTile, n > 0);  // dK += dS^T Q
-        mma_commit(&bars->x_empty[st]);
+        mma_commit_e(&bars->x_empty[st]);
         if (n + 1 < niter) issue_dp(n + 1);  // dS^T_n is read by the dK MMAs queued above
       }
-      if (ok) mma_commit(&bars->acc_full);
-      mma_commit(&bars->drain);
+      if (ok) mma_commit_e(&bars->acc_full);
+      mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
   } else {
@@ -556,30 +556,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, BK, false, false);  // K-major x K-major, N = 128
       constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sQ = sbase + C::kOffRes0;
       const uint32_t sdO = sbase + C::kOffRes1;
       auto issue_s = [&](int n) -> bool {  // S_n = Q K_n^T into buffer n & 1
         const int st = n % C::kKStages;
-        if (!wait_bar(&bars->x_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
+        if (!warp_wait(&bars->x_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
         issue_kk<D>(tmem + C::kTmS + (n & 1) * 128, sQ, C::kChunk, sbase + C::kOffK + st * C::kTile, C::kChunk,
                     idesc_s);
-        mma_commit(&bars->s_full[n & 1]);
+        mma_commit_e(&bars->s_full[n & 1]);
         return true;
       };
       auto issue_dp = [&](int n) -> bool {  // dP_n = dO V_n^T; its V stage is free once this completes
         const int st = n % C::kVStages;
-        if (!wait_bar(&bars->v_full[st], (n / C::kVStages) & 1, ctl, kCode)) return false;
+        if (!warp_wait(&bars->v_full[st], (n / C::kVStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
         issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffV + st * C::kTile, C::kChunk, idesc_s);
-        mma_commit(&bars->dp_full[0]);
-        mma_commit(&bars->v_empty[st]);
+        mma_commit_e(&bars->dp_full[0]);
+        mma_commit_e(&bars->v_empty[st]);
         return true;
       };
-      bool ok = wait_bar(&bars->res_full, 0, ctl, kCode);
+      bool ok = warp_wait(&bars->res_full, 0, ctl, kCode);
       if (ok && nblk > 0) {
         ok = issue_s(0);
         if (ok) ok = issue_dp(0);
@@ -588,19 +588,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok && n < nblk; ++n) {
         if (n + 1 < nblk && !(ok = issue_s(n + 1))) break;
         const int st = n % C::kKStages;
-        if (!(ok = wait_bar(&bars->ds_full[0], n & 1, ctl, kCode))) break;
+        if (!(ok = warp_wait(&bars->ds_full[0], n & 1, ctl, kCode))) break;
         tc_fence_after();
         if (n + 1 < nblk && !(ok = issue_dp(n + 1))) break;  // dP_n has been read: its columns are free
         // dQ += dS K   (K = the block's 128 key rows)
         const uint64_t b0 = sdesc_sw128(sbase + C::kOffK + st * C::kTile, C::kChunk, 1024);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma_ts(tmem + C::kTmDQ, tmem + C::kTmS + (n & 1) * 128 + packed_slice_col128(kk),
+          mma_ts_e(tmem + C::kTmDQ, tmem + C::kTmS + (n & 1) * 128 + packed_slice_col128(kk),
                  b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bars->x_empty[st]);
+        mma_commit_e(&bars->x_empty[st]);
       }
-      if (ok) mma_commit(&bars->acc_full);
-      mma_commit(&bars->drain);
+      if (ok) mma_commit_e(&bars->acc_full);
+      mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
   } else {

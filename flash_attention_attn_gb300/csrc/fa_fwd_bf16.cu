@@ -168,15 +168,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 5) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_f32acc<F16>(128, D, false, true);
-      bool ok = wait_bar(&bars->q_tmem, 0, ctl, kCode);
+      bool ok = warp_wait(&bars->q_tmem, 0, ctl, kCode);
       for (int n = 0; ok && n <= nblk; ++n) {
         if (n < nblk) {
           const int st = n % C::kStages;
           const int sb = n & 1;
-          if (!(ok = wait_bar(&bars->k_full[st], (n / C::kStages) & 1, ctl, kCode))) break;
+          if (!(ok = warp_wait(&bars->k_full[st], (n / C::kStages) & 1, ctl, kCode))) break;
           tc_fence_after();
           const uint32_t sk = sbase + C::kOffK + st * C::kTileBytes;
           // descriptors built once, stepped by (bytes >> 4) in the address field
@@ -184,32 +184,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-            mma_ts(tmem + C::kTmS + sb * 128, tmem + C::kTmQ + kk * 8, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
+            mma_ts_e(tmem + C::kTmS + sb * 128, tmem + C::kTmQ + kk * 8, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&bars->s_full[sb]);
-          mma_commit(&bars->k_empty[st]);
+          mma_commit_e(&bars->s_full[sb]);
+          mma_commit_e(&bars->k_empty[st]);
         }
         if (n >= 1) {
           const int m = n - 1;
           const int st = m % C::kStages;
           const int sb = m & 1;
-          if (!(ok = wait_bar(&bars->p_full[sb], (m >> 1) & 1, ctl, kCode))) break;
-          if (!(ok = wait_bar(&bars->v_full[st], (m / C::kStages) & 1, ctl, kCode))) break;
+          if (!(ok = warp_wait(&bars->p_full[sb], (m >> 1) & 1, ctl, kCode))) break;
+          if (!(ok = warp_wait(&bars->v_full[st], (m / C::kStages) & 1, ctl, kCode))) break;
           tc_fence_after();
           const uint32_t sv = sbase + C::kOffV + st * C::kTileBytes;
           const uint64_t vdesc = sdesc_sw128(sv, C::kChunkBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             // P: 16 bf16 keys per step = 8 TMEM columns; V: 16 key rows = 2048 bytes
-            mma_ts(tmem + C::kTmO, tmem + C::kTmS + sb * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
+            mma_ts_e(tmem + C::kTmO, tmem + C::kTmS + sb * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
                    (m > 0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars->o_done);
-          mma_commit(&bars->v_empty[st]);
+          mma_commit_e(&bars->o_done);
+          mma_commit_e(&bars->v_empty[st]);
         }
       }
       // every MMA this thread issued must finish before TMEM is released
-      mma_commit(&bars->drain);
+      mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
   } else {
@@ -498,7 +498,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, 128, false, false);  // Q x K^T, both K-major
       constexpr uint32_t idesc_o = idesc_f32acc<F16>(128, D, false, true);     // P (TMEM) x V (MN-major)
       int n_s[2] = {0, 0};  // S MMAs issued per tile (s_full phases)
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       auto issue_s = [&](int t, int n) -> bool {  // S_t = Q_t K_n^T
         const int st = n % C::kKStages;
         if (k_seen < n) {
-          if (!wait_bar(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
+          if (!warp_wait(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
           tc_fence_after();
           k_seen = n;
         }
@@ -517,42 +517,42 @@ __global__ void __launch_bounds__(kThreads2, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::kTmS + t * 128, qdesc + off, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
+          mma_ss_e(tmem + C::kTmS + t * 128, qdesc + off, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bars->s_full[t]);
+        mma_commit_e(&bars->s_full[t]);
         ++n_s[t];
         return true;
       };
-      bool ok = wait_bar(&bars->q_full, 0, ctl, kCode);
+      bool ok = warp_wait(&bars->q_full, 0, ctl, kCode);
       if (ok && nblk > 0) {
         for (int t = 0; ok && t < 2; ++t)
           if (in_tile(t, lo)) ok = issue_s(t, 0);
-        if (ok) mma_commit(&bars->k_empty[0]);
+        if (ok) mma_commit_e(&bars->k_empty[0]);
       }
       for (int n = 0; ok && n < nblk; ++n) {
         const int kb = lo + n;
         const int stv = n % C::kVStages;
-        if (!(ok = wait_bar(&bars->v_full[stv], (n / C::kVStages) & 1, ctl, kCode))) break;
+        if (!(ok = warp_wait(&bars->v_full[stv], (n / C::kVStages) & 1, ctl, kCode))) break;
         const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + stv * C::kTileBytes, C::kChunkBytes, 1024);
         for (int t = 0; ok && t < 2; ++t) {
           if (in_tile(t, kb)) {
-            if (!(ok = wait_bar(&bars->p_full[t], n_p[t] & 1, ctl, kCode))) break;
+            if (!(ok = warp_wait(&bars->p_full[t], n_p[t] & 1, ctl, kCode))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
-              mma_ts(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
+              mma_ts_e(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
                      (n_p[t] > 0 || kk > 0) ? 1u : 0u);
-            if (kb == (t ? hi_b : hi_a)) mma_commit(&bars->o_done[t]);  // the tile's last PV
+            if (kb == (t ? hi_b : hi_a)) mma_commit_e(&bars->o_done[t]);  // the tile's last PV
             ++n_p[t];
           }
           if (n + 1 < nblk && in_tile(t, kb + 1)) ok = issue_s(t, n + 1);
         }
         if (!ok) break;
-        mma_commit(&bars->v_empty[stv]);
-        if (n + 1 < nblk) mma_commit(&bars->k_empty[(n + 1) % C::kKStages]);
+        mma_commit_e(&bars->v_empty[stv]);
+        if (n + 1 < nblk) mma_commit_e(&bars->k_empty[(n + 1) % C::kKStages]);
       }
       // every MMA this thread issued must finish before TMEM is released
-      mma_commit(&bars->drain);
+      mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
   } else {
