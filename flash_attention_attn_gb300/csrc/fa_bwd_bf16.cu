@@ -262,14 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n >= C::kStages && !warp_wait(&bars->x_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
       const int h = g * rep + n / nqb;
       const int qb = qlo + n % nqb;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->x_full[st], 2 * C::kTile);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
+      mbar_arrive_expect_tx_e(&bars->x_full[st], 2 * C::kTile);  // one elected lane arms and copies
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d_e(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
                       qb * BQ, b);
-          tma_load_4d(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
+        tma_load_4d_e(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
                       qb * BQ, b);
-        }
       }
       float* rows = srows + st * 256;
 #pragma unroll
@@ -513,47 +511,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr unsigned kCode = 4u;  // FA_DEVERR_DQ_TIMEOUT
 
   if (warp == 8) {
-    // lane 0 streams K (and loads Q, dO once), lane 1 streams V: separate
-    // rings, so a V wait never holds back the next K load
+    // the whole warp streams K and V through separate rings (a V stage is
+    // freed after its dP MMA, a K stage only after its dQ MMA), in the order
+    // the MMAs need them; one elected lane arms each barrier and issues each copy
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
-        tma_load_4d(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
-      }
-      int issued = 0;
-      for (int n = 0; n < nblk; ++n) {
-        const int st = n % C::kKStages;
-        if (n >= C::kKStages && !wait_bar(&bars->x_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx(&bars->x_full[st], C::kTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmK, &bars->x_full[st], smem + C::kOffK + st * C::kTile + c * C::kChunk, c * 64, g,
+    }
+    mbar_arrive_expect_tx_e(&bars->res_full, 2 * C::kTile);
+    for (int c = 0; c < C::kChunks; ++c) {
+      tma_load_4d_e(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
+      tma_load_4d_e(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
+    }
+    int issued_k = 0, issued_v = 0;
+    for (int n = 0; n < nblk; ++n) {
+      const int sk = n % C::kKStages;
+      if (n >= C::kKStages && !warp_wait(&bars->x_empty[sk], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
+      mbar_arrive_expect_tx_e(&bars->x_full[sk], C::kTile);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d_e(&tmK, &bars->x_full[sk], smem + C::kOffK + sk * C::kTile + c * C::kChunk, c * 64, g,
                       (kb_lo + n) * BK, b);
-        issued = n + 1;
-      }
-      if (bars->abort) {
-        drain_bar(&bars->res_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued - C::kKStages); n < issued; ++n)
-          drain_bar(&bars->x_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
-      }
-    } else if (lane == 1) {
-      int issued = 0;
-      for (int n = 0; n < nblk; ++n) {
-        const int st = n % C::kVStages;
-        if (n >= C::kVStages && !wait_bar(&bars->v_empty[st], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTile);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmV, &bars->v_full[st], smem + C::kOffV + st * C::kTile + c * C::kChunk, c * 64, g,
+      issued_k = n + 1;
+      const int sv = n % C::kVStages;
+      if (n >= C::kVStages && !warp_wait(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
+      mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTile);
+      for (int c = 0; c < C::kChunks; ++c)
+        tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTile + c * C::kChunk, c * 64, g,
                       (kb_lo + n) * BK, b);
-        issued = n + 1;
-      }
-      if (bars->abort)
-        for (int n = imax(0, issued - C::kVStages); n < issued; ++n)
-          drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
+      issued_v = n + 1;
+    }
+    if (bars->abort) {
+      drain_bar(&bars->res_full, 0, p.timeout_ns);
+      for (int n = imax(0, issued_k - C::kKStages); n < issued_k; ++n)
+        drain_bar(&bars->x_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
+      for (int n = imax(0, issued_v - C::kVStages); n < issued_v; ++n)
+        drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     {  // the whole warp runs the loop; one elected lane issues

@@ -131,30 +131,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !p.inject_stall) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+    // the whole warp runs the loop; one elected lane arms each barrier and
+    // issues each copy
+    if (!p.inject_stall) {
+      if (lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+      }
+      mbar_arrive_expect_tx_e(&bars->q_full, C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d(&tmQ, &bars->q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, h, qb * kBM, b);
+        tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, h, qb * kBM, b);
       int issued = 0;
       for (int n = 0; n < nblk; ++n) {
         const int st = n % C::kStages;
         const int kb = kb_lo + n;
         uint8_t* sk = smem + C::kOffK + st * C::kTileBytes;
         uint8_t* sv = smem + C::kOffV + st * C::kTileBytes;
-        if (n >= C::kStages && !wait_bar(&bars->k_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        if (n >= C::kStages && !warp_wait(&bars->k_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx_e(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
-        if (n >= C::kStages && !wait_bar(&bars->v_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) {
+          tma_load_4d_e(&tmK, &bars->k_full[st], sk + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
+        if (n >= C::kStages && !warp_wait(&bars->v_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) {
           drain_bar(&bars->k_full[st], (n / C::kStages) & 1, p.timeout_ns);
           break;
         }
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+        mbar_arrive_expect_tx_e(&bars->v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
+          tma_load_4d_e(&tmV, &bars->v_full[st], sv + c * C::kChunkBytes, c * 64, g, kb * kBN, b);
         issued = n + 1;
       }
       if (bars->abort) {
@@ -461,29 +465,33 @@ __global__ void __launch_bounds__(kThreads2, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !p.inject_stall) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
+    // the whole warp runs the loop; one elected lane arms each barrier and
+    // issues each copy
+    if (!p.inject_stall) {
+      if (lane == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+      }
+      mbar_arrive_expect_tx_e(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
       for (int t = 0; t < (has_b ? 2 : 1); ++t)
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64, h,
+          tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64, h,
                       (2 * pair + t) * kBM, b);
       int issued_k = 0, issued_v = 0;
       for (int n = 0; n < nblk; ++n) {
         const int st = n % C::kKStages;
-        if (n >= C::kKStages && !wait_bar(&bars->k_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+        if (n >= C::kKStages && !warp_wait(&bars->k_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx_e(&bars->k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
+          tma_load_4d_e(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
                       c * 64, g, (lo + n) * kBN, b);
         issued_k = n + 1;
         const int sv = n % C::kVStages;
-        if (n >= C::kVStages && !wait_bar(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx(&bars->v_full[sv], C::kTileBytes);
+        if (n >= C::kVStages && !warp_wait(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
+        mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
+          tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
                       c * 64, g, (lo + n) * kBN, b);
         issued_v = n + 1;
       }
