@@ -31,7 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, make_inputs, torch_dtype  # noqa: E402
 
 METRIC = "attention TFLOP/s fwd and fwd+bwd (causal GQA bf16) and % of BF16 tensor peak"
 DEFAULT_WORKLOAD = 5
@@ -251,6 +251,49 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def measure_prologue(w: Workload, dev, reps: int = 10):
+    """Device time of the pre-attention prologue (QK RMS-norm + rotary,
+    forward and backward) on this workload's shape: tokens = B*T, hq = H,
+    hk = HKV query/key heads of the packed projection, RoPE factors of base
+    10000.  HBM-bound: bytes = what each kernel must read and write."""
+    import torch
+    import flash_attention_attn_gb300 as fa
+    if w.dtype not in ("bf16", "fp16") or w.D not in (64, 128):
+        return None
+    dt = torch_dtype(w.dtype)
+    tokens = w.B * w.T
+    gen = torch.Generator(device=dev).manual_seed(1000 + w.wid)
+    qk = torch.randn((tokens, w.H + w.HKV, w.D), generator=gen, device=dev).to(dt)
+    pos = torch.arange(w.T, device=dev).repeat(w.B).float()
+    inv = 10000.0 ** (-torch.arange(0, w.D, 2, device=dev).float() / w.D)
+    theta = pos[:, None] * inv[None, :]
+    f1 = torch.repeat_interleave(torch.cos(theta), 2, dim=1).contiguous()
+    f2 = torch.stack([-torch.sin(theta), torch.sin(theta)], dim=2).reshape(tokens, w.D).contiguous()
+    q, k = fa.qk_norm_rope_fwd(qk, f1, f2, w.H)
+    dq = torch.randn(q.shape, generator=gen, device=dev).to(dt)
+    dk = torch.randn(k.shape, generator=gen, device=dev).to(dt)
+    dqk = fa.qk_norm_rope_bwd(dq, dk, qk, f1, f2)
+    out = {}
+    elem = qk.element_size()
+    fbytes = 2 * f1.numel() * 4
+    for name, fn, nbytes in (
+            ("fwd", lambda: fa.qk_norm_rope_fwd(qk, f1, f2, w.H, q=q, k=k), (qk.numel() + q.numel() + k.numel()) * elem + fbytes),
+            ("bwd", lambda: fa.qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk=dqk),
+             (dq.numel() + dk.numel() + qk.numel() + dqk.numel()) * elem + fbytes)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        out[name] = {"ms": ms, "bytes": nbytes, "achieved_gbs": nbytes / (ms / 1e3) / 1e9}
+    return out
+
+
 def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
     import torch
     import flash_attention_attn_gb300 as fa
@@ -356,8 +399,9 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "ms_per_step": 1e3 * e2e_s / e2e_steps}
 
+    prologue = None if args.no_prologue else measure_prologue(w, dev)
     return {"per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
-            "e2e": e2e, "elem_bytes": q.element_size()}
+            "e2e": e2e, "elem_bytes": q.element_size(), "prologue": prologue}
 
 
 def workload_from_args(args) -> Workload:
@@ -388,6 +432,7 @@ def main():
     ap.add_argument("--ref-T", type=int, default=4096, help="sequence prefix per reference-arm step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prologue", action="store_true", help="skip the QK-norm + rotary prologue measurement")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.shape:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -482,6 +527,10 @@ def main():
         "e2e": r["e2e"],
         "device": torch.cuda.get_device_name(0),
     }
+    if r["prologue"] is not None:
+        # outside the timed step: the QK-norm + rotary prologue on the same shape (HBM-bound)
+        line["prologue"] = {n: dict(v, peak_gbs=peaks["hbm_gbs"], frac=v["achieved_gbs"] / peaks["hbm_gbs"])
+                            for n, v in r["prologue"].items()}
     if cpu is not None:
         t = cpu["seconds"][0]
         line["cpu_baseline"] = {

@@ -32,11 +32,15 @@ from ._binding import (  # noqa: F401
     fa_plan_block_mask,
     fa_plan_kv_range,
     fa_plan_q_range,
+    fa_qk_norm_rope_bwd,
+    fa_qk_norm_rope_fwd,
     fa_status_string,
     fa_tile_m,
     fa_tile_n,
     fa_workspace_size,
     load,
+    qk_norm_rope_bwd,
+    qk_norm_rope_fwd,
 )
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -91,6 +91,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_debug_config.restype = _i
         lib.fa_debug_fwd_tiles.argtypes = [_i]
         lib.fa_debug_fwd_tiles.restype = _i
+        lib.fa_qk_norm_rope_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_vp]
+        lib.fa_qk_norm_rope_fwd.restype = _i
+        lib.fa_qk_norm_rope_bwd.argtypes = [_vp] * 6 + [_i] * 5 + [_vp]
+        lib.fa_qk_norm_rope_bwd.restype = _i
         _lib = lib
         return lib
 
@@ -176,6 +180,14 @@ def fa_debug_config(wait_timeout_ns: int = 0, inject_stall: int = 0) -> int:
 
 def fa_debug_fwd_tiles(tiles: int = 0) -> int:
     return load().fa_debug_fwd_tiles(int(tiles))
+
+
+def fa_qk_norm_rope_fwd(qk, f1, f2, q, k, tokens, hq, hk, head_dim, dtype, stream) -> int:
+    return load().fa_qk_norm_rope_fwd(qk, f1, f2, q, k, tokens, hq, hk, head_dim, dtype, stream)
+
+
+def fa_qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk, tokens, hq, hk, head_dim, dtype, stream) -> int:
+    return load().fa_qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk, tokens, hq, hk, head_dim, dtype, stream)
 
 
 # ------------------------------------------------------------ torch layer
@@ -296,3 +308,47 @@ def check_status(device=None, stream=None, op: int = FA_OP_BWD) -> tuple[int, in
             if st != FA_OK:
                 worst = (st, word)
     return worst
+
+
+def qk_norm_rope_fwd(qk, f1, f2, hq, q=None, k=None, stream=None):
+    """Pre-attention prologue: q [tokens, hq, D] and k [tokens, hk, D] from the
+    packed projection qk [tokens, hq + hk, D] (bf16 or fp16) and the fp32
+    rotary factors f1, f2 [tokens, D]: RMS-norm of every head vector, then
+    y_d = f1_d n_d + f2_d n_(d xor 1)."""
+    torch = _torch()
+    tokens, heads, D = qk.shape
+    hk = heads - int(hq)
+    dev = qk.device
+    dt = _dtype_code(qk)
+    for name, t in (("f1", f1), ("f2", f2)):
+        _check_tensor(name, t, (tokens, D), torch.float32, dev)
+    q = torch.empty((tokens, hq, D), dtype=qk.dtype, device=dev) if q is None else q
+    k = torch.empty((tokens, hk, D), dtype=qk.dtype, device=dev) if k is None else k
+    _check_tensor("qk", qk, (tokens, heads, D), qk.dtype, dev)
+    _check_tensor("q", q, (tokens, hq, D), qk.dtype, dev)
+    _check_tensor("k", k, (tokens, hk, D), qk.dtype, dev)
+    st = fa_qk_norm_rope_fwd(qk.data_ptr(), f1.data_ptr(), f2.data_ptr(), q.data_ptr(), k.data_ptr(), tokens,
+                             int(hq), hk, D, dt, _stream(dev, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_qk_norm_rope_fwd")
+    return q, k
+
+
+def qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk=None, stream=None):
+    """Gradient of the packed projection qk given the gradients of q and k."""
+    torch = _torch()
+    tokens, heads, D = qk.shape
+    hq, hk = dq.shape[1], dk.shape[1]
+    dev = qk.device
+    dt = _dtype_code(qk)
+    _check_tensor("dq", dq, (tokens, hq, D), qk.dtype, dev)
+    _check_tensor("dk", dk, (tokens, hk, D), qk.dtype, dev)
+    for name, t in (("f1", f1), ("f2", f2)):
+        _check_tensor(name, t, (tokens, D), torch.float32, dev)
+    dqk = torch.empty_like(qk) if dqk is None else dqk
+    _check_tensor("dqk", dqk, (tokens, heads, D), qk.dtype, dev)
+    st = fa_qk_norm_rope_bwd(dq.data_ptr(), dk.data_ptr(), qk.data_ptr(), f1.data_ptr(), f2.data_ptr(),
+                             dqk.data_ptr(), tokens, hq, hk, D, dt, _stream(dev, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_qk_norm_rope_bwd")
+    return dqk

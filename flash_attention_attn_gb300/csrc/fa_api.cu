@@ -53,6 +53,7 @@ size_t delta_bytes(int B, int T, int H) { return round_up(sizeof(float) * static
 struct DeviceInfo {
   bool probed = false;
   bool sm103 = false;
+  int sms = 0;
 };
 
 std::mutex g_mu;
@@ -71,6 +72,7 @@ int device_ok(int* dev_out) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FA_ERR_CUDA;
     d.sm103 = (major == 10 && minor == 3);
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
     d.probed = true;
   }
   *dev_out = dev;
@@ -323,6 +325,37 @@ int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* 
 int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb) {
   if (T < 1 || BM < 1 || BN < 1 || window < 0 || qb < 0 || kb < 0) return -FA_ERR_INVALID_ARG;
   return fa::block_needs_mask(T, BM, BN, causal, window, qb, kb) ? 1 : 0;
+}
+
+int fa_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens, int hq,
+                        int hk, int head_dim, int dtype, void* stream) {
+  if (tokens < 1 || hq < 1 || hk < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(tokens) * (hq + hk) * head_dim >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
+  const void* ptrs[5] = {qk, f1, f2, q, k};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  int dev, st;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  return status_of(fa::launch_qk_norm_rope_fwd(qk, f1, f2, q, k, tokens, hq, hk, head_dim, dtype == FA_DTYPE_FP16,
+                                               g_dev[dev].sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2, void* dqk,
+                        int tokens, int hq, int hk, int head_dim, int dtype, void* stream) {
+  if (tokens < 1 || hq < 1 || hk < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(tokens) * (hq + hk) * head_dim >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
+  const void* ptrs[6] = {dq, dk, qk, f1, f2, dqk};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  int dev, st;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  return status_of(fa::launch_qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk, tokens, hq, hk, head_dim,
+                                               dtype == FA_DTYPE_FP16, g_dev[dev].sms,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 int fa_tile_m(void) { return fa::kBM; }

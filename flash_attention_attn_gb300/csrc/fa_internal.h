@@ -97,6 +97,12 @@ struct TensorMaps {
 };
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
+// Pre-attention prologue (RMS-norm + rotary of the packed QK projection).
+cudaError_t launch_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens,
+                                    int hq, int hk, int D, bool f16, int sms, cudaStream_t stream);
+cudaError_t launch_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2,
+                                    void* dqk, int tokens, int hq, int hk, int D, bool f16, int sms,
+                                    cudaStream_t stream);
 // Whether the bf16 forward runs two query tiles per CTA for this shape.
 bool fwd_two_tiles(const Shape& s);
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);

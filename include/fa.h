@@ -203,6 +203,36 @@ int fa_plan_kv_range(int T, int BM, int BN, int causal, int window, int qb, int*
 int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* lo, int* hi);
 int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb);
 
+/*
+ * Pre-attention prologue: RMS-norm of every query and key head vector of the
+ * packed QK projection, then the rotary mix with per-position factors, as the
+ * modded-nanogpt page qkv_rope.py defines it (`_qk_norm_rope_forward_kernel`,
+ * without its paired-heads and key-offset options):
+ *
+ *   x = qk[t][c][:] ;  rstd = 1 / sqrt(mean_d x_d^2 + 2^-23) ;  n = rstd x
+ *   y_d = f1[t][d] n_d + f2[t][d] n_(d xor 1)
+ *
+ * qk      [tokens][hq + hk][head_dim] 16-bit (dtype bf16 or fp16): heads
+ *         c < hq are queries, the next hk are keys (hq = hk in the page; any
+ *         hk >= 1 here, so that GQA keys can be produced).
+ * f1, f2  [tokens][head_dim] fp32 rotary factors (cos / signed sin, or any).
+ * q       [tokens][hq][head_dim], k [tokens][hk][head_dim], same dtype:
+ *         with tokens = B*T these are the [B,T,H,D] / [B,T,HKV,D] tensors
+ *         fa_fwd reads.
+ * The backward (the norm/rotary part of the page's
+ * `_qkv_norm_rope_pack_fp8_backward_kernel`, without the fp8 packing) takes
+ * the gradients dq, dk of q and k and writes dqk, the gradient of qk:
+ *   gn_e = f1[t][e] g_e + f2[t][e xor 1] g_(e xor 1)
+ *   dx_e = rstd (gn_e - n_e mean_d(gn_d n_d))
+ * head_dim 64 or 128; every pointer 16-byte aligned (else
+ * FA_ERR_INVALID_ARG); fp32 arithmetic.  Asynchronous on `stream`; the
+ * caller owns every buffer.
+ */
+int fa_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens, int hq,
+                        int hk, int head_dim, int dtype, void* stream);
+int fa_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2, void* dqk,
+                        int tokens, int hq, int hk, int head_dim, int dtype, void* stream);
+
 /* Tile sizes the bf16 kernels use (query rows, key rows per block). */
 int fa_tile_m(void);
 int fa_tile_n(void);

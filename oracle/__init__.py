@@ -68,9 +68,12 @@ def _bind(lib):
     lib.oracle_attn_dkdv_rows.argtypes = [_D, _D, _D, _D] + common + [
         ctypes.c_int, ctypes.c_int, _I, ctypes.c_int, _D, _D]
     lib.oracle_triu_offsets.argtypes = [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]
+    lib.oracle_qk_norm_rope_fwd.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 4
+    lib.oracle_qk_norm_rope_bwd.argtypes = [_D, _D, _D, _D, _D, _D] + [ctypes.c_int] * 4
     for name in ("oracle_attn_probs", "oracle_attn_fwd", "oracle_attn_bwd",
                  "oracle_attn_fwd_rows", "oracle_attn_dq_rows",
-                 "oracle_attn_dkdv_rows", "oracle_triu_offsets"):
+                 "oracle_attn_dkdv_rows", "oracle_triu_offsets",
+                 "oracle_qk_norm_rope_fwd", "oracle_qk_norm_rope_bwd"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -233,3 +236,31 @@ def triu_offsets(num_rows: int, num_cols: int) -> list[int]:
     if n < 0 or n > cap:
         raise RuntimeError(f"oracle_triu_offsets({num_rows}, {num_cols}) returned {n}")
     return [out[i] for i in range(n)]
+
+
+def qk_norm_rope_fwd(qk, f1, f2, hq: int):
+    """Pre-attention prologue: (q [tokens, hq, D], k [tokens, hk, D]) from the
+    packed projection qk [tokens, hq + hk, D] and the rotary factors
+    f1, f2 [tokens, D]: RMS-norm of every head vector, then
+    y_d = f1_d n_d + f2_d n_(d xor 1)."""
+    qk, f1, f2 = _f64(qk), _f64(f1), _f64(f2)
+    tokens, heads, D = qk.shape
+    hk = heads - int(hq)
+    q = np.empty((tokens, hq, D), np.float64)
+    k = np.empty((tokens, hk, D), np.float64)
+    _check(_load().oracle_qk_norm_rope_fwd(_p(qk), _p(f1), _p(f2), _p(q), _p(k), tokens, int(hq), hk, D),
+           "oracle_qk_norm_rope_fwd")
+    return q, k
+
+
+def qk_norm_rope_bwd(dq, dk, qk, f1, f2):
+    """Gradient of the packed projection qk given the gradients of q and k."""
+    dq, dk, qk, f1, f2 = _f64(dq), _f64(dk), _f64(qk), _f64(f1), _f64(f2)
+    tokens, heads, D = qk.shape
+    hq, hk = dq.shape[1], dk.shape[1]
+    if hq + hk != heads:
+        raise ValueError("dq and dk heads do not add up to qk's")
+    dqk = np.empty_like(qk)
+    _check(_load().oracle_qk_norm_rope_bwd(_p(dq), _p(dk), _p(qk), _p(f1), _p(f2), _p(dqk), tokens, hq, hk, D),
+           "oracle_qk_norm_rope_bwd")
+    return dqk

@@ -479,3 +479,76 @@ int oracle_triu_offsets(int numRows, int numCols, int* out, int cap) {
   }
   return count;
 }
+
+/* ------------------------------------------------------------------------
+ * Pre-attention prologue: RMS-norm of every query and key head vector, then
+ * the rotary mix with per-position factors, as the modded-nanogpt page
+ * qkv_rope.py defines it (module docstring and `_qk_norm_rope_forward_kernel`,
+ * read without its "paired heads" and "key offset" options; the fp8 packing
+ * of its backward kernel is left out).  Input: the packed projection
+ * qk[t][c][d], t < tokens, heads c < hq are queries and hq <= c < hq + hk are
+ * keys, d < D (D even); factors f1[t][d], f2[t][d].
+ *
+ *   ms   = (1/D) sum_d x_d^2 ;  rstd = 1 / sqrt(ms + eps),  eps = 2^-23
+ *   n_d  = rstd x_d
+ *   y_d  = f1[t][d] n_d + f2[t][d] n_{d xor 1}      (partner: the other lane
+ *                                                     of the pair (2i, 2i+1))
+ *
+ * Queries go to q[t][c][d], keys to k[t][c - hq][d].  The backward takes the
+ * gradients g of q and k and returns the gradient of qk: by the chain rule
+ * through y (dL/dn_e = f1_e g_e + f2_{e xor 1} g_{e xor 1}) and through the
+ * RMS-norm,
+ *
+ *   gn_e = f1[t][e] g_e + f2[t][e xor 1] g_{e xor 1}
+ *   dx_e = rstd (gn_e - n_e (1/D) sum_d gn_d n_d)
+ * ------------------------------------------------------------------------ */
+static const double kQkEps = 1.1920928955078125e-7;
+
+static double qk_rstd(const double* x, int D) {
+  double ms = 0.0;
+  for (int d = 0; d < D; ++d) ms += x[d] * x[d];
+  ms /= D;
+  return 1.0 / sqrt(ms + kQkEps);
+}
+
+int oracle_qk_norm_rope_fwd(const double* qk, const double* f1, const double* f2, double* q, double* k,
+                            int tokens, int hq, int hk, int D) {
+  if (tokens < 1 || hq < 1 || hk < 1 || D < 2 || D % 2) return 1;
+  const int heads = hq + hk;
+#pragma omp parallel for schedule(static)
+  for (long t = 0; t < tokens; ++t) {
+    for (int c = 0; c < heads; ++c) {
+      const double* x = qk + ((size_t)t * heads + c) * D;
+      double* y = c < hq ? q + ((size_t)t * hq + c) * D : k + ((size_t)t * hk + (c - hq)) * D;
+      const double rstd = qk_rstd(x, D);
+      for (int d = 0; d < D; ++d)
+        y[d] = f1[(size_t)t * D + d] * (x[d] * rstd) + f2[(size_t)t * D + d] * (x[d ^ 1] * rstd);
+    }
+  }
+  return 0;
+}
+
+int oracle_qk_norm_rope_bwd(const double* dq, const double* dk, const double* qk, const double* f1,
+                            const double* f2, double* dqk, int tokens, int hq, int hk, int D) {
+  if (tokens < 1 || hq < 1 || hk < 1 || D < 2 || D % 2) return 1;
+  const int heads = hq + hk;
+#pragma omp parallel for schedule(static)
+  for (long t = 0; t < tokens; ++t) {
+    double* gn = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int c = 0; c < heads; ++c) {
+      const double* x = qk + ((size_t)t * heads + c) * D;
+      const double* g = c < hq ? dq + ((size_t)t * hq + c) * D : dk + ((size_t)t * hk + (c - hq)) * D;
+      double* dx = dqk + ((size_t)t * heads + c) * D;
+      const double rstd = qk_rstd(x, D);
+      double corr = 0.0;
+      for (int e = 0; e < D; ++e) {
+        gn[e] = f1[(size_t)t * D + e] * g[e] + f2[(size_t)t * D + (e ^ 1)] * g[e ^ 1];
+        corr += gn[e] * (x[e] * rstd);
+      }
+      corr /= D;
+      for (int e = 0; e < D; ++e) dx[e] = rstd * (gn[e] - (x[e] * rstd) * corr);
+    }
+    free(gn);
+  }
+  return 0;
+}

@@ -122,7 +122,41 @@ def _pin_finite_differences():
     return True
 
 
-PINS = {"sdpa+lse": _pin_sdpa, "rows": _pin_rows_match_full, "triu": _pin_triu, "fd": _pin_finite_differences}
+def _pin_prologue():
+    """QK-norm + rotary: rotation as complex multiplication, unit RMS under
+    identity factors, and the backward against finite differences."""
+    rng = np.random.default_rng(8)
+    tokens, hq, hk, D = 3, 2, 1, 4
+    qk = rng.standard_normal((tokens, hq + hk, D))
+    ones, zeros = np.ones((tokens, D)), np.zeros((tokens, D))
+    n = np.concatenate(oracle.qk_norm_rope_fwd(qk, ones, zeros, hq), axis=1)
+    ms = np.mean(qk ** 2, axis=-1)
+    if not np.allclose(np.mean(n ** 2, axis=-1), ms / (ms + 1.1920928955078125e-7), rtol=1e-12):
+        return False
+    theta = rng.uniform(-3, 3, size=(tokens, D // 2))
+    f1 = np.repeat(np.cos(theta), 2, axis=1)
+    f2 = np.stack([-np.sin(theta), np.sin(theta)], axis=2).reshape(tokens, D)
+    y = np.concatenate(oracle.qk_norm_rope_fwd(qk, f1, f2, hq), axis=1)
+    z = (n[..., 0::2] + 1j * n[..., 1::2]) * np.exp(1j * theta)[:, None, :]
+    if not (np.allclose(y[..., 0::2], z.real, atol=1e-12) and np.allclose(y[..., 1::2], z.imag, atol=1e-12)):
+        return False
+    f1, f2 = rng.standard_normal((tokens, D)), rng.standard_normal((tokens, D))
+    gq, gk = rng.standard_normal((tokens, hq, D)), rng.standard_normal((tokens, hk, D))
+    dqk = oracle.qk_norm_rope_bwd(gq, gk, qk, f1, f2)
+    h = 1e-6
+    for idx in np.ndindex(qk.shape):
+        xp, xm = qk.copy(), qk.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        lp = sum(float(np.sum(a * g)) for a, g in zip(oracle.qk_norm_rope_fwd(xp, f1, f2, hq), (gq, gk)))
+        lm = sum(float(np.sum(a * g)) for a, g in zip(oracle.qk_norm_rope_fwd(xm, f1, f2, hq), (gq, gk)))
+        if abs((lp - lm) / (2 * h) - dqk[idx]) > 1e-6 * max(1.0, abs(dqk[idx])):
+            return False
+    return True
+
+
+PINS = {"sdpa+lse": _pin_sdpa, "rows": _pin_rows_match_full, "triu": _pin_triu, "fd": _pin_finite_differences,
+        "prologue": _pin_prologue}
 
 
 def _failing_pins():
@@ -155,6 +189,10 @@ MUTANTS = [
     ("P transposed in dK/dV", "const double p = P[(size_t)i * T + j];", "const double p = P[(size_t)j * T + i];", 0),
     ("dP reads the wrong V row", "dot(doi, V + kv_index(s, b, j, g), s->D)", "dot(doi, V + kv_index(s, b, i, g), s->D)", 0),
     ("triu wrap too small", "if (k > numCols - 1) k -= numRows + numCols;", "if (k > numCols - 1) k -= numCols;", 0),
+    ("prologue partner d+1", "(x[d ^ 1] * rstd)", "(x[(d + 1) % D] * rstd)", 0),
+    ("prologue eps dropped", "return 1.0 / sqrt(ms + kQkEps);", "return 1.0 / sqrt(ms);", 0),
+    ("prologue norm correction dropped", "dx[e] = rstd * (gn[e] - (x[e] * rstd) * corr);", "dx[e] = rstd * gn[e];", 0),
+    ("prologue grad partner factor", "f2[(size_t)t * D + (e ^ 1)] * g[e ^ 1]", "f2[(size_t)t * D + e] * g[e ^ 1]", 0),
     ("row LSE missing in dq rows", "softmax_row(P, T);\n        dp_row(&s, V, dO, b, h, i, dP);\n        double delta",
      "dp_row(&s, V, dO, b, h, i, dP);\n        double delta", 0),
 ]
