@@ -163,6 +163,38 @@ def test_forward_tiles_per_cta(case, tiles):
     check_fwd(w, got["o"], O, got["lse"], LSE)
 
 
+def _random_cases(n=16, seed=2026):
+    """Seeded random shapes across the supported space: dtype, batch, GQA
+    ratio, ragged lengths, head dims 16..128, causal or not, windows."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        hkv = int(rng.choice([1, 2, 4]))
+        h = hkv * int(rng.choice([1, 2, 4]))
+        T = int(rng.integers(1, 700))
+        D = int(rng.choice([16, 32, 48, 64, 72, 96, 128]))
+        causal = bool(rng.random() < 0.75)
+        window = int(rng.choice([0, 0, 1, 17, 128, 300]))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        cases.append((dtype, int(rng.integers(1, 3)), h, hkv, T, D, window, causal))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "-".join(map(str, c)))
+def test_random_shapes_elementwise(case):
+    dtype, B, H, HKV, T, D, window, causal = case
+    w = Workload(104, "random", dtype, B, H, HKV, T, D, window, causal, True, "normal")
+    inp = make_inputs(w, seed=3000 + T + D + H)
+    got = run_gpu(w, inp)
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    O, LSE = oracle.fwd(Q, K, V, w.scale, causal, window)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, causal, window)
+    check_fwd(w, got["o"], O, got["lse"], LSE)
+    check_grad(w, "dQ", got["dq"], dQ)
+    check_grad(w, "dK", got["dk"], dK)
+    check_grad(w, "dV", got["dv"], dV)
+
+
 def test_backward_is_bitwise_reproducible():
     w = Workload(101, "repro", "bf16", 1, 8, 2, 640, 128, 0, True, True, "normal")
     inp = make_inputs(w, seed=7)
