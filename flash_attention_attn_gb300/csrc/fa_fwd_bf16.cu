@@ -582,9 +582,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const int kb = lo_own + j;
       if (!(ok = warp_wait(&bars->s_full[t], j & 1, ctl, kCode))) break;
       tc_fence_after();
-      // The loops below are kept rolled over 32-column chunks: fully unrolled,
-      // this softmax did not fit the instruction cache next to the other
-      // roles and ran several times slower.
+      // The masking pre-pass stays rolled over 32-column chunks: unrolled with
+      // everything else, this softmax did not fit the instruction cache next
+      // to the other roles and ran several times slower.
       if (block_needs_mask(s.T, kBM, kBN, s.causal, s.window, q, kb)) {
         // rare (diagonal, window-edge and tail blocks): -inf over the masked
         // scores in TMEM, so that both passes below stay mask-free
@@ -600,19 +600,26 @@ __global__ void __launch_bounds__(kThreads2, 1)
         }
         tmem_st_wait();
       }
+      // One TMEM round trip per block: the row's 128 scores stay in registers
+      // for both passes (re-reading them for pass 2 cost two more load
+      // latencies on the softmax's critical path).
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(s_addr, s0);
+      tmem_ld32(s_addr + 32, s1);
+      tmem_ld32(s_addr + 64, s2);
+      tmem_ld32(s_addr + 96, s3);
+      tmem_ld_wait(s0);
+      reg_tie(s1);
+      reg_tie(s2);
+      reg_tie(s3);
       // pass 1: row max over eight independent partials
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-#pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(s_addr + c2 * 64, ra);
-        tmem_ld32(s_addr + c2 * 64 + 32, rb);
-        tmem_ld_wait(ra);
-        reg_tie(rb);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) mx8[c & 7] = fmax3(mx8[c & 7], __uint_as_float(ra[c]), __uint_as_float(rb[c]));
+      for (int c = 0; c < 32; ++c) {
+        mx8[c & 7] = fmax3(mx8[c & 7], __uint_as_float(s0[c]), __uint_as_float(s1[c]));
+        mx8[(c + 4) & 7] = fmax3(mx8[(c + 4) & 7], __uint_as_float(s2[c]), __uint_as_float(s3[c]));
       }
       float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
@@ -623,36 +630,34 @@ __global__ void __launch_bounds__(kThreads2, 1)
       const float m_ref = (first || resc) ? m_new : m_run;
       const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
       // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
-      // 64 columns of S_t (step c writes columns [32c, 32c+32), which only
-      // steps <= c have read).  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
-      // - (m, m) in one instruction; the sum in four packed partials.
+      // 64 columns of S_t.  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
+      // - (m, m) in one instruction; the sum in two packed partials.
       const uint64_t sl2x2 = f2_pack(sl2, sl2);
       const uint64_t negm2 = f2_pack(-m_use, -m_use);
-      uint64_t sum4[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {  // 64 columns per step: two loads in flight
-        uint32_t ra[64];
-        tmem_ld32(s_addr + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
-        tmem_ld32(s_addr + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
-        tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&ra[0]));
-        reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&ra[32]));
-        uint32_t pk[32];
+      uint64_t sum2[2] = {0ull, 0ull};
+      // 32 scores -> 16 packed columns of P, stored as soon as they are formed
+      // so that each quarter's registers free up for the next
+      auto exp_quarter = [&](const uint32_t(&a)[32], uint32_t col) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(ra[2 * e]), __uint_as_float(ra[2 * e + 1])), sl2x2, negm2);
+        for (int e = 0; e < 16; ++e) {
+          const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])), sl2x2, negm2);
           float x0, x1;
           f2_unpack(x01, x0, x1);
           const float p0 = ex2(x0), p1 = ex2(x1);
-          sum4[e & 3] = f2_add(sum4[e & 3], f2_pack(p0, p1));
+          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
           pk[e] = pack2<F16>(p0, p1);
         }
-        tmem_st32(s_addr + c2 * 32, pk);
-      }
+        tmem_st16(s_addr + col, pk);
+      };
+      exp_quarter(s0, 0);
+      exp_quarter(s1, 16);
+      exp_quarter(s2, 32);
+      exp_quarter(s3, 48);
       tmem_st_wait();
-      float a0, a1, b0, b1;
-      f2_unpack(f2_add(sum4[0], sum4[1]), a0, a1);
-      f2_unpack(f2_add(sum4[2], sum4[3]), b0, b1);
-      const float sum = (a0 + b0) + (a1 + b1);
+      float a0, a1;
+      f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
+      const float sum = a0 + a1;
       if (!first && __any_sync(0xffffffffu, resc)) {
         // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order pipe)
         const float corr = resc ? ex2(m_run - m_new) : 1.f;
