@@ -399,7 +399,8 @@ struct Bars2 {
   uint64_t v_full[4];
   uint64_t v_empty[4];  // V stage free once the PV MMAs of both tiles completed
   uint64_t s_full[2];   // per tile
-  uint64_t p_full[2];   // per tile: one arrival per softmax warp
+  uint64_t p_half[2];   // per tile: keys 0-63 of P stored (and O rescaled), one arrival per softmax warp
+  uint64_t p_full[2];   // per tile: keys 64-127 of P stored, one arrival per softmax warp
   uint64_t o_done[2];   // per tile: all its PV MMAs completed (committed once, after the last)
   uint64_t drain;
   uint32_t tmem_base;
@@ -445,6 +446,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_half[t], 4);
       mbar_init(&bars->p_full[t], 4);
       mbar_init(&bars->o_done[t], 1);
     }
@@ -544,12 +546,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
         const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + stv * C::kTileBytes, C::kChunkBytes, 1024);
         for (int t = 0; ok && t < 2; ++t) {
           if (in_tile(t, kb)) {
-            if (!(ok = warp_wait(&bars->p_full[t], n_p[t] & 1, ctl, kCode))) break;
-            tc_fence_after();
+            // P arrives in two halves of 64 keys: the first half's MMAs run
+            // while the softmax still forms the second
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
-              mma_ts_e(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4), idesc_o,
-                     (n_p[t] > 0 || kk > 0) ? 1u : 0u);
+            for (int hf = 0; hf < 2; ++hf) {
+              if (!(ok = warp_wait(hf ? &bars->p_full[t] : &bars->p_half[t], n_p[t] & 1, ctl, kCode))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int k4 = 0; k4 < kBN / 32; ++k4) {  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
+                const int kk = hf * (kBN / 32) + k4;
+                mma_ts_e(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4),
+                         idesc_o, (n_p[t] > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
             if (kb == (t ? hi_b : hi_a)) mma_commit_e(&bars->o_done[t]);  // the tile's last PV
             ++n_p[t];
           }
@@ -652,14 +662,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
       };
       exp_quarter(s0, 0);
       exp_quarter(s1, 16);
-      exp_quarter(s2, 32);
-      exp_quarter(s3, 48);
-      tmem_st_wait();
-      float a0, a1;
-      f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
-      const float sum = a0 + a1;
       if (!first && __any_sync(0xffffffffu, resc)) {
-        // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order pipe)
+        // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order
+        // pipe); rescaled before the first half of P is released to PV_t(j)
         const float corr = resc ? ex2(m_run - m_new) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
@@ -670,11 +675,18 @@ __global__ void __launch_bounds__(kThreads2, 1)
           for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
           tmem_st32(o_addr + c * 32, ro);
         }
-        tmem_st_wait();
         if (resc) l_run *= corr;
       }
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive(&bars->p_half[t]);
+      exp_quarter(s2, 32);
+      exp_quarter(s3, 48);
+      tmem_st_wait();
+      float a0, a1;
+      f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
       if (first || resc) m_run = m_new;
-      l_run += sum;
+      l_run += a0 + a1;
       tc_fence_before();
       warp_arrive(&bars->p_full[t]);
     }
