@@ -67,6 +67,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 512, "one-tile barriers exceed their shared-memory slot");
 
 __device__ __forceinline__ void reg_tie(uint32_t (&r)[32]) {
   asm volatile(""
@@ -406,6 +407,8 @@ struct Bars2 {
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(Bars2) <= 512, "two-tile barriers exceed their shared-memory slot");
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads2, 1)
