@@ -8,9 +8,9 @@ The arithmetic lives in ``attn_oracle.c`` (plain C, IEEE double); this module
 compiles it with gcc into ``oracle/_build/`` and wraps it with ctypes + numpy.
 Every function takes and returns float64 numpy arrays in the layouts
 
-    Q, O, dO, dQ : [B, T, H,   D]
-    K, V, dK, dV : [B, T, HKV, D]
-    LSE, Delta   : [B, H, T]
+    Q, O, dO, dQ : [B, Tq, H,   D]
+    K, V, dK, dV : [B, Tk, HKV, D]      (Tk = Tq for self-attention)
+    LSE, Delta   : [B, H, Tq]
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, library routines, finite differences, the printed triu
@@ -57,7 +57,7 @@ def build(force: bool = False) -> str:
 
 
 def _bind(lib):
-    common = [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    common = [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int, ctypes.c_int]  # B, Tq, Tk, H, HKV, D, ...
     lib.oracle_attn_probs.argtypes = [_D, _D] + common + [ctypes.c_int, ctypes.c_int, _D, _D]
     lib.oracle_attn_fwd.argtypes = [_D, _D, _D] + common + [_D, _D]
     lib.oracle_attn_bwd.argtypes = [_D, _D, _D, _D] + common + [_D, _D, _D, _D]
@@ -128,11 +128,12 @@ def _p(a: np.ndarray):
 
 
 def _shape(Q, K):
+    """(B, Tq, Tk, H, HKV, D); queries and keys may differ in length."""
     B, T, H, D = Q.shape
     Bk, Tk, HKV, Dk = K.shape
-    if (Bk, Tk, Dk) != (B, T, D):
+    if (Bk, Dk) != (B, D):
         raise ValueError(f"Q {Q.shape} and K {K.shape} disagree")
-    return B, T, H, HKV, D
+    return B, T, Tk, H, HKV, D
 
 
 def _check(rc: int, what: str):
@@ -141,24 +142,26 @@ def _check(rc: int, what: str):
 
 
 def probs(Q, K, scale, causal, window, b, h):
-    """Full T x T probability matrix P of one (b, h), and its LSE row."""
+    """Full Tq x Tk probability matrix P of one (b, h), and its LSE row."""
     Q, K = _f64(Q), _f64(K)
-    B, T, H, HKV, D = _shape(Q, K)
-    P = np.empty((T, T), np.float64)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
+    P = np.empty((T, Tk), np.float64)
     lse = np.empty((T,), np.float64)
-    _check(_load().oracle_attn_probs(_p(Q), _p(K), B, T, H, HKV, D, float(scale),
+    _check(_load().oracle_attn_probs(_p(Q), _p(K), B, T, Tk, H, HKV, D, float(scale),
                                      int(causal), int(window), int(b), int(h),
                                      _p(P), _p(lse)), "oracle_attn_probs")
     return P, lse
 
 
 def fwd(Q, K, V, scale, causal, window):
-    """(O [B,T,H,D], LSE [B,H,T]) by the plain definition."""
+    """(O [B,Tq,H,D], LSE [B,H,Tq]) by the plain definition."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
-    B, T, H, HKV, D = _shape(Q, K)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
+    if V.shape != K.shape:
+        raise ValueError(f"K {K.shape} and V {V.shape} disagree")
     O = np.empty_like(Q)
     LSE = np.empty((B, H, T), np.float64)
-    _check(_load().oracle_attn_fwd(_p(Q), _p(K), _p(V), B, T, H, HKV, D, float(scale),
+    _check(_load().oracle_attn_fwd(_p(Q), _p(K), _p(V), B, T, Tk, H, HKV, D, float(scale),
                                    int(causal), int(window), _p(O), _p(LSE)),
            "oracle_attn_fwd")
     return O, LSE
@@ -167,12 +170,14 @@ def fwd(Q, K, V, scale, causal, window):
 def bwd(Q, K, V, dO, scale, causal, window):
     """(dQ, dK, dV, Delta) by the analytic gradient of the definition."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
-    B, T, H, HKV, D = _shape(Q, K)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
+    if V.shape != K.shape or dO.shape != Q.shape:
+        raise ValueError("V must match K and dO must match Q")
     dQ = np.empty_like(Q)
     dK = np.empty_like(K)
     dV = np.empty_like(V)
     Delta = np.empty((B, H, T), np.float64)
-    _check(_load().oracle_attn_bwd(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+    _check(_load().oracle_attn_bwd(_p(Q), _p(K), _p(V), _p(dO), B, T, Tk, H, HKV, D,
                                    float(scale), int(causal), int(window),
                                    _p(dQ), _p(dK), _p(dV), _p(Delta)),
            "oracle_attn_bwd")
@@ -189,11 +194,11 @@ def _rows(rows, T):
 def fwd_rows(Q, K, V, scale, causal, window, b, h, rows):
     """O rows [n, D] and LSE [n] of query rows `rows` of one (b, h)."""
     Q, K, V = _f64(Q), _f64(K), _f64(V)
-    B, T, H, HKV, D = _shape(Q, K)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
     r = _rows(rows, T)
     O = np.empty((r.size, D), np.float64)
     L = np.empty((r.size,), np.float64)
-    _check(_load().oracle_attn_fwd_rows(_p(Q), _p(K), _p(V), B, T, H, HKV, D, float(scale),
+    _check(_load().oracle_attn_fwd_rows(_p(Q), _p(K), _p(V), B, T, Tk, H, HKV, D, float(scale),
                                         int(causal), int(window), int(b), int(h),
                                         r.ctypes.data_as(_I), r.size, _p(O), _p(L)),
            "oracle_attn_fwd_rows")
@@ -203,11 +208,11 @@ def fwd_rows(Q, K, V, scale, causal, window, b, h, rows):
 def dq_rows(Q, K, V, dO, scale, causal, window, b, h, rows):
     """dQ rows [n, D] and Delta [n] of query rows `rows` of one (b, h)."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
-    B, T, H, HKV, D = _shape(Q, K)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
     r = _rows(rows, T)
     dq = np.empty((r.size, D), np.float64)
     de = np.empty((r.size,), np.float64)
-    _check(_load().oracle_attn_dq_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+    _check(_load().oracle_attn_dq_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, Tk, H, HKV, D,
                                        float(scale), int(causal), int(window), int(b), int(h),
                                        r.ctypes.data_as(_I), r.size, _p(dq), _p(de)),
            "oracle_attn_dq_rows")
@@ -217,11 +222,11 @@ def dq_rows(Q, K, V, dO, scale, causal, window, b, h, rows):
 def dkdv_rows(Q, K, V, dO, scale, causal, window, b, g, cols):
     """dK rows and dV rows [n, D] of key rows `cols` of one (b, kv head g)."""
     Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
-    B, T, H, HKV, D = _shape(Q, K)
-    c = _rows(cols, T)
+    B, T, Tk, H, HKV, D = _shape(Q, K)
+    c = _rows(cols, Tk)
     dk = np.empty((c.size, D), np.float64)
     dv = np.empty((c.size, D), np.float64)
-    _check(_load().oracle_attn_dkdv_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, H, HKV, D,
+    _check(_load().oracle_attn_dkdv_rows(_p(Q), _p(K), _p(V), _p(dO), B, T, Tk, H, HKV, D,
                                          float(scale), int(causal), int(window), int(b), int(g),
                                          c.ctypes.data_as(_I), c.size, _p(dk), _p(dv)),
            "oracle_attn_dkdv_rows")

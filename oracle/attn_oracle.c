@@ -29,6 +29,13 @@
  * O = 0 and LSE = 0, the guard of the same kernel's epilogue (it cannot occur
  * for self-attention, where j = i is always visible).
  *
+ * Queries and keys may differ in length (Tq query rows i, Tk key rows j):
+ * the teeny-kernels page (flash_attn2.rs, `flash_attention2_forward`) takes
+ * separate n_ctx_q and n_ctx_k and visits every key of every query row.  The
+ * visibility rule above is applied as written for any (i, j); the CUDA path
+ * accepts Tq != Tk only without causal or window masking, where it is
+ * unconditional.
+ *
  * Backward (the analytic gradient of the definition above; the same formulas
  * appear in the Graphcore page's `flashAttentionQKVPackedGrad`, the
  * teeny-kernels page flash_attn2.rs `flash_attention2_backward_dq` /
@@ -47,9 +54,9 @@
  * OpenMP only spreads independent rows / columns over cores.
  *
  * Layouts (row-major, contiguous):
- *   Q, O, dO, dQ : [B, T, H,   D]
- *   K, V, dK, dV : [B, T, HKV, D]
- *   LSE, Delta   : [B, H, T]
+ *   Q, O, dO, dQ : [B, Tq, H,   D]
+ *   K, V, dK, dV : [B, Tk, HKV, D]
+ *   LSE, Delta   : [B, H, Tq]
  */
 #include <math.h>
 #include <stdlib.h>
@@ -60,9 +67,10 @@
 #define ORACLE_ENOMEM 2
 
 typedef struct {
-  int B, T, H, HKV, D;
+  int B, T, H, HKV, D; /* T: query rows */
   double scale;
   int causal, window;
+  int Tk; /* key rows */
 } shape_t;
 
 static int visible(const shape_t* s, long i, long j) {
@@ -76,7 +84,7 @@ static size_t q_index(const shape_t* s, long b, long t, long h) {
 }
 
 static size_t kv_index(const shape_t* s, long b, long t, long g) {
-  return (((size_t)b * s->T + t) * s->HKV + g) * s->D;
+  return (((size_t)b * s->Tk + t) * s->HKV + g) * s->D;
 }
 
 static size_t row_index(const shape_t* s, long b, long h, long t) {
@@ -84,7 +92,7 @@ static size_t row_index(const shape_t* s, long b, long h, long t) {
 }
 
 static int check_shape(const shape_t* s) {
-  if (s->B < 1 || s->T < 1 || s->H < 1 || s->HKV < 1 || s->D < 1) return 0;
+  if (s->B < 1 || s->T < 1 || s->Tk < 1 || s->H < 1 || s->HKV < 1 || s->D < 1) return 0;
   if (s->H % s->HKV != 0) return 0;
   if (s->window < 0) return 0;
   return 1;
@@ -101,7 +109,7 @@ static void score_row(const shape_t* s, const double* Q, const double* K,
                       long b, long h, long i, double* S_row) {
   const long g = h / (s->H / s->HKV);
   const double* qi = Q + q_index(s, b, i, h);
-  for (long j = 0; j < s->T; ++j) {
+  for (long j = 0; j < s->Tk; ++j) {
     if (visible(s, i, j))
       S_row[j] = s->scale * dot(qi, K + kv_index(s, b, j, g), s->D);
     else
@@ -110,20 +118,20 @@ static void score_row(const shape_t* s, const double* Q, const double* K,
 }
 
 /*
- * Three-pass softmax of one score row, in place: S_row becomes P_row.
+ * Three-pass softmax of one score row of n keys, in place: S_row becomes P_row.
  * Returns LSE = m + ln l, or 0 for a row with no visible key (then P_row = 0).
  */
-static double softmax_row(double* S_row, long T) {
+static double softmax_row(double* S_row, long n) {
   double m = -INFINITY;
-  for (long j = 0; j < T; ++j)
+  for (long j = 0; j < n; ++j)
     if (S_row[j] > m) m = S_row[j];
   if (m == -INFINITY) {
-    for (long j = 0; j < T; ++j) S_row[j] = 0.0;
+    for (long j = 0; j < n; ++j) S_row[j] = 0.0;
     return 0.0;
   }
   double l = 0.0;
-  for (long j = 0; j < T; ++j) l += exp(S_row[j] - m);
-  for (long j = 0; j < T; ++j) S_row[j] = exp(S_row[j] - m) / l;
+  for (long j = 0; j < n; ++j) l += exp(S_row[j] - m);
+  for (long j = 0; j < n; ++j) S_row[j] = exp(S_row[j] - m) / l;
   return m + log(l);
 }
 
@@ -132,53 +140,53 @@ static void dp_row(const shape_t* s, const double* V, const double* dO,
                    long b, long h, long i, double* dP_row) {
   const long g = h / (s->H / s->HKV);
   const double* doi = dO + q_index(s, b, i, h);
-  for (long j = 0; j < s->T; ++j)
+  for (long j = 0; j < s->Tk; ++j)
     dP_row[j] = visible(s, i, j) ? dot(doi, V + kv_index(s, b, j, g), s->D) : 0.0;
 }
 
 /* ------------------------------------------------------------------ forward */
 
 /*
- * Full probability matrix of one (b, h): P[i*T + j].  Also LSE_head[i] if not
- * NULL.  This is the unfused T x T matrix the flash method avoids; the oracle
- * materialises it on purpose.
+ * Full probability matrix of one (b, h): P[i*Tk + j].  Also LSE_head[i] if
+ * not NULL.  This is the unfused Tq x Tk matrix the flash method avoids; the
+ * oracle materialises it on purpose.
  */
 int oracle_attn_probs(const double* Q, const double* K,
-                      int B, int T, int H, int HKV, int D,
+                      int B, int T, int Tk, int H, int HKV, int D,
                       double scale, int causal, int window,
                       int b, int h, double* P, double* LSE_head) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
 #pragma omp parallel for schedule(dynamic, 16)
   for (long i = 0; i < T; ++i) {
-    double* row = P + (size_t)i * T;
+    double* row = P + (size_t)i * Tk;
     score_row(&s, Q, K, b, h, i, row);
-    const double lse = softmax_row(row, T);
+    const double lse = softmax_row(row, Tk);
     if (LSE_head) LSE_head[i] = lse;
   }
   return ORACLE_OK;
 }
 
-/* O = P V and LSE for every (b, h), one head's T x T matrix at a time. */
+/* O = P V and LSE for every (b, h), one head's Tq x Tk matrix at a time. */
 int oracle_attn_fwd(const double* Q, const double* K, const double* V,
-                    int B, int T, int H, int HKV, int D,
+                    int B, int T, int Tk, int H, int HKV, int D,
                     double scale, int causal, int window,
                     double* O, double* LSE) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s)) return ORACLE_EINVAL;
-  double* P = (double*)malloc(sizeof(double) * (size_t)T * T);
+  double* P = (double*)malloc(sizeof(double) * (size_t)T * Tk);
   if (!P) return ORACLE_ENOMEM;
   for (int b = 0; b < B; ++b) {
     for (int h = 0; h < H; ++h) {
       const long g = h / (H / HKV);
-      oracle_attn_probs(Q, K, B, T, H, HKV, D, scale, causal, window, b, h, P,
+      oracle_attn_probs(Q, K, B, T, Tk, H, HKV, D, scale, causal, window, b, h, P,
                         LSE + row_index(&s, b, h, 0));
 #pragma omp parallel for schedule(dynamic, 16)
       for (long i = 0; i < T; ++i) {
         double* oi = O + q_index(&s, b, i, h);
         for (int d = 0; d < D; ++d) oi[d] = 0.0;
-        for (long j = 0; j < T; ++j) {
-          const double p = P[(size_t)i * T + j];
+        for (long j = 0; j < Tk; ++j) {
+          const double p = P[(size_t)i * Tk + j];
           if (p == 0.0) continue;
           const double* vj = V + kv_index(&s, b, j, g);
           for (int d = 0; d < D; ++d) oi[d] += p * vj[d];
@@ -195,18 +203,18 @@ int oracle_attn_fwd(const double* Q, const double* K, const double* V,
 /*
  * dQ, dK, dV (and Delta, if not NULL) for every (b, h).  Per KV head g the
  * rep query heads of its group are visited in order and their dK / dV
- * contributions summed.  Materialises P and dS (T x T each) per head.
+ * contributions summed.  Materialises P and dS (Tq x Tk each) per head.
  */
 int oracle_attn_bwd(const double* Q, const double* K, const double* V,
                     const double* dO,
-                    int B, int T, int H, int HKV, int D,
+                    int B, int T, int Tk, int H, int HKV, int D,
                     double scale, int causal, int window,
                     double* dQ, double* dK, double* dV, double* Delta) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s)) return ORACLE_EINVAL;
   const int rep = H / HKV;
-  double* P = (double*)malloc(sizeof(double) * (size_t)T * T);
-  double* dS = (double*)malloc(sizeof(double) * (size_t)T * T);
+  double* P = (double*)malloc(sizeof(double) * (size_t)T * Tk);
+  double* dS = (double*)malloc(sizeof(double) * (size_t)T * Tk);
   if (!P || !dS) {
     free(P);
     free(dS);
@@ -214,26 +222,26 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V,
   }
   for (int b = 0; b < B; ++b) {
     for (int g = 0; g < HKV; ++g) {
-      for (long j = 0; j < T; ++j) {
+      for (long j = 0; j < Tk; ++j) {
         memset(dK + kv_index(&s, b, j, g), 0, sizeof(double) * D);
         memset(dV + kv_index(&s, b, j, g), 0, sizeof(double) * D);
       }
       for (int r = 0; r < rep; ++r) {
         const int h = g * rep + r;
-        oracle_attn_probs(Q, K, B, T, H, HKV, D, scale, causal, window, b, h, P, NULL);
+        oracle_attn_probs(Q, K, B, T, Tk, H, HKV, D, scale, causal, window, b, h, P, NULL);
         /* rows: dP, Delta, dS, dQ */
 #pragma omp parallel for schedule(dynamic, 16)
         for (long i = 0; i < T; ++i) {
-          const double* Pi = P + (size_t)i * T;
-          double* dSi = dS + (size_t)i * T;
+          const double* Pi = P + (size_t)i * Tk;
+          double* dSi = dS + (size_t)i * Tk;
           dp_row(&s, V, dO, b, h, i, dSi); /* dSi holds dP_i for now */
           double delta = 0.0;
-          for (long j = 0; j < T; ++j) delta += Pi[j] * dSi[j];
+          for (long j = 0; j < Tk; ++j) delta += Pi[j] * dSi[j];
           if (Delta) Delta[row_index(&s, b, h, i)] = delta;
-          for (long j = 0; j < T; ++j) dSi[j] = Pi[j] * (dSi[j] - delta);
+          for (long j = 0; j < Tk; ++j) dSi[j] = Pi[j] * (dSi[j] - delta);
           double* dqi = dQ + q_index(&s, b, i, h);
           for (int d = 0; d < D; ++d) dqi[d] = 0.0;
-          for (long j = 0; j < T; ++j) {
+          for (long j = 0; j < Tk; ++j) {
             if (dSi[j] == 0.0) continue;
             const double* kj = K + kv_index(&s, b, j, g);
             for (int d = 0; d < D; ++d) dqi[d] += dSi[j] * kj[d];
@@ -242,12 +250,12 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V,
         }
         /* columns: dK_j += scale * dS^T Q, dV_j += P^T dO (one thread per j) */
 #pragma omp parallel for schedule(dynamic, 16)
-        for (long j = 0; j < T; ++j) {
+        for (long j = 0; j < Tk; ++j) {
           double* dkj = dK + kv_index(&s, b, j, g);
           double* dvj = dV + kv_index(&s, b, j, g);
           for (long i = 0; i < T; ++i) {
-            const double p = P[(size_t)i * T + j];
-            const double ds = dS[(size_t)i * T + j];
+            const double p = P[(size_t)i * Tk + j];
+            const double ds = dS[(size_t)i * Tk + j];
             const double* qi = Q + q_index(&s, b, i, h);
             const double* doi = dO + q_index(&s, b, i, h);
             if (ds != 0.0)
@@ -272,11 +280,11 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V,
  * that outputs of a large problem can be checked one by one.
  */
 int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
-                         int B, int T, int H, int HKV, int D,
+                         int B, int T, int Tk, int H, int HKV, int D,
                          double scale, int causal, int window,
                          int b, int h, const int* rows, int nrows,
                          double* O_rows, double* LSE_rows) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
   for (int n = 0; n < nrows; ++n)
     if (rows[n] < 0 || rows[n] >= T) return ORACLE_EINVAL;
@@ -284,7 +292,7 @@ int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
   int status = ORACLE_OK;
 #pragma omp parallel
   {
-    double* P = (double*)malloc(sizeof(double) * (size_t)T);
+    double* P = (double*)malloc(sizeof(double) * (size_t)Tk);
     if (!P) {
 #pragma omp atomic write
       status = ORACLE_ENOMEM;
@@ -293,10 +301,10 @@ int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
       for (int n = 0; n < nrows; ++n) {
         const long i = rows[n];
         score_row(&s, Q, K, b, h, i, P);
-        LSE_rows[n] = softmax_row(P, T);
+        LSE_rows[n] = softmax_row(P, Tk);
         double* oi = O_rows + (size_t)n * D;
         for (int d = 0; d < D; ++d) oi[d] = 0.0;
-        for (long j = 0; j < T; ++j) {
+        for (long j = 0; j < Tk; ++j) {
           if (P[j] == 0.0) continue;
           const double* vj = V + kv_index(&s, b, j, g);
           for (int d = 0; d < D; ++d) oi[d] += P[j] * vj[d];
@@ -311,11 +319,11 @@ int oracle_attn_fwd_rows(const double* Q, const double* K, const double* V,
 /* dQ (and Delta) of selected query rows of one (b, h). */
 int oracle_attn_dq_rows(const double* Q, const double* K, const double* V,
                         const double* dO,
-                        int B, int T, int H, int HKV, int D,
+                        int B, int T, int Tk, int H, int HKV, int D,
                         double scale, int causal, int window,
                         int b, int h, const int* rows, int nrows,
                         double* dQ_rows, double* Delta_rows) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s) || b < 0 || b >= B || h < 0 || h >= H) return ORACLE_EINVAL;
   for (int n = 0; n < nrows; ++n)
     if (rows[n] < 0 || rows[n] >= T) return ORACLE_EINVAL;
@@ -323,8 +331,8 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V,
   int status = ORACLE_OK;
 #pragma omp parallel
   {
-    double* P = (double*)malloc(sizeof(double) * (size_t)T);
-    double* dP = (double*)malloc(sizeof(double) * (size_t)T);
+    double* P = (double*)malloc(sizeof(double) * (size_t)Tk);
+    double* dP = (double*)malloc(sizeof(double) * (size_t)Tk);
     if (!P || !dP) {
 #pragma omp atomic write
       status = ORACLE_ENOMEM;
@@ -333,14 +341,14 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V,
       for (int n = 0; n < nrows; ++n) {
         const long i = rows[n];
         score_row(&s, Q, K, b, h, i, P);
-        softmax_row(P, T);
+        softmax_row(P, Tk);
         dp_row(&s, V, dO, b, h, i, dP);
         double delta = 0.0;
-        for (long j = 0; j < T; ++j) delta += P[j] * dP[j];
+        for (long j = 0; j < Tk; ++j) delta += P[j] * dP[j];
         if (Delta_rows) Delta_rows[n] = delta;
         double* dqi = dQ_rows + (size_t)n * D;
         for (int d = 0; d < D; ++d) dqi[d] = 0.0;
-        for (long j = 0; j < T; ++j) {
+        for (long j = 0; j < Tk; ++j) {
           const double ds = P[j] * (dP[j] - delta);
           if (ds == 0.0) continue;
           const double* kj = K + kv_index(&s, b, j, g);
@@ -362,14 +370,14 @@ int oracle_attn_dq_rows(const double* Q, const double* K, const double* V,
  */
 int oracle_attn_dkdv_rows(const double* Q, const double* K, const double* V,
                           const double* dO,
-                          int B, int T, int H, int HKV, int D,
+                          int B, int T, int Tk, int H, int HKV, int D,
                           double scale, int causal, int window,
                           int b, int g, const int* cols, int ncols,
                           double* dK_rows, double* dV_rows) {
-  shape_t s = {B, T, H, HKV, D, scale, causal, window};
+  shape_t s = {B, T, H, HKV, D, scale, causal, window, Tk};
   if (!check_shape(&s) || b < 0 || b >= B || g < 0 || g >= HKV) return ORACLE_EINVAL;
   for (int n = 0; n < ncols; ++n)
-    if (cols[n] < 0 || cols[n] >= T) return ORACLE_EINVAL;
+    if (cols[n] < 0 || cols[n] >= Tk) return ORACLE_EINVAL;
   const int rep = H / HKV;
   memset(dK_rows, 0, sizeof(double) * (size_t)ncols * D);
   memset(dV_rows, 0, sizeof(double) * (size_t)ncols * D);
@@ -395,8 +403,8 @@ int oracle_attn_dkdv_rows(const double* Q, const double* K, const double* V,
     const int h = g * rep + r;
 #pragma omp parallel
     {
-      double* P = (double*)malloc(sizeof(double) * (size_t)T);
-      double* dP = (double*)malloc(sizeof(double) * (size_t)T);
+      double* P = (double*)malloc(sizeof(double) * (size_t)Tk);
+      double* dP = (double*)malloc(sizeof(double) * (size_t)Tk);
       if (!P || !dP) {
 #pragma omp atomic write
         status = ORACLE_ENOMEM;
@@ -405,10 +413,10 @@ int oracle_attn_dkdv_rows(const double* Q, const double* K, const double* V,
         for (long i = 0; i < T; ++i) {
           if (!need[i]) continue;
           score_row(&s, Q, K, b, h, i, P);
-          softmax_row(P, T);
+          softmax_row(P, Tk);
           dp_row(&s, V, dO, b, h, i, dP);
           double delta = 0.0;
-          for (long j = 0; j < T; ++j) delta += P[j] * dP[j];
+          for (long j = 0; j < Tk; ++j) delta += P[j] * dP[j];
           for (int n = 0; n < ncols; ++n) {
             const long j = cols[n];
             Psel[(size_t)i * ncols + n] = P[j];

@@ -155,8 +155,38 @@ def _pin_prologue():
     return True
 
 
+def _pin_cross():
+    """Tq != Tk (fewer queries than keys, so that a planted length mix-up
+    stays inside the buffers): torch float64 SDPA + autograd, and the
+    sampled-row functions against the full ones."""
+    rng = np.random.default_rng(9)
+    for (B, Tq, Tk, H, HKV, D) in ((2, 3, 8, 4, 2, 3), (1, 5, 7, 2, 1, 4)):
+        Q, K, V, dO = (rng.standard_normal(s) for s in ((B, Tq, H, D), (B, Tk, HKV, D), (B, Tk, HKV, D), (B, Tq, H, D)))
+        O, LSE = oracle.fwd(Q, K, V, 0.6, False, 0)
+        dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, 0.6, False, 0)
+        q, k, v = (torch.tensor(x).permute(0, 2, 1, 3).requires_grad_(True) for x in (Q, K, V))
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=0.6, enable_gqa=True)
+        o.backward(torch.tensor(dO).permute(0, 2, 1, 3))
+        refs = [o.detach()] + [t.grad for t in (q, k, v)]
+        for a, r in zip((O, dQ, dK, dV), refs):
+            if not np.allclose(a, r.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-10):
+                return False
+        cols = [0, Tk - 1]
+        for h in range(H):
+            o_r, l_r = oracle.fwd_rows(Q, K, V, 0.6, False, 0, 0, h, [Tq - 1])
+            dq_r, _ = oracle.dq_rows(Q, K, V, dO, 0.6, False, 0, 0, h, [Tq - 1])
+            if not (np.allclose(o_r, O[0, [Tq - 1], h], atol=1e-12) and np.allclose(l_r, LSE[0, h, [Tq - 1]], atol=1e-12)
+                    and np.allclose(dq_r, dQ[0, [Tq - 1], h], atol=1e-12)):
+                return False
+        for g in range(HKV):
+            dk_r, dv_r = oracle.dkdv_rows(Q, K, V, dO, 0.6, False, 0, 0, g, cols)
+            if not (np.allclose(dk_r, dK[0, cols, g], atol=1e-12) and np.allclose(dv_r, dV[0, cols, g], atol=1e-12)):
+                return False
+    return True
+
+
 PINS = {"sdpa+lse": _pin_sdpa, "rows": _pin_rows_match_full, "triu": _pin_triu, "fd": _pin_finite_differences,
-        "prologue": _pin_prologue}
+        "prologue": _pin_prologue, "cross": _pin_cross}
 
 
 def _failing_pins():
@@ -186,14 +216,22 @@ MUTANTS = [
      "const double* kj = V + kv_index(&s, b, j, g);\n            for (int d = 0; d < D; ++d) dqi[d]", 0),
     ("dK without scale", "dkj[d] += scale * ds * qi[d];", "dkj[d] += ds * qi[d];", 0),
     ("dV from dS", "for (int d = 0; d < D; ++d) dvj[d] += p * doi[d];", "for (int d = 0; d < D; ++d) dvj[d] += ds * doi[d];", 0),
-    ("P transposed in dK/dV", "const double p = P[(size_t)i * T + j];", "const double p = P[(size_t)j * T + i];", 0),
+    ("P transposed in dK/dV", "const double p = P[(size_t)i * Tk + j];", "const double p = P[(size_t)j * Tk + i];", 0),
     ("dP reads the wrong V row", "dot(doi, V + kv_index(s, b, j, g), s->D)", "dot(doi, V + kv_index(s, b, i, g), s->D)", 0),
     ("triu wrap too small", "if (k > numCols - 1) k -= numRows + numCols;", "if (k > numCols - 1) k -= numCols;", 0),
     ("prologue partner d+1", "(x[d ^ 1] * rstd)", "(x[(d + 1) % D] * rstd)", 0),
     ("prologue eps dropped", "return 1.0 / sqrt(ms + kQkEps);", "return 1.0 / sqrt(ms);", 0),
     ("prologue norm correction dropped", "dx[e] = rstd * (gn[e] - (x[e] * rstd) * corr);", "dx[e] = rstd * gn[e];", 0),
     ("prologue grad partner factor", "f2[(size_t)t * D + (e ^ 1)] * g[e ^ 1]", "f2[(size_t)t * D + e] * g[e ^ 1]", 0),
-    ("row LSE missing in dq rows", "softmax_row(P, T);\n        dp_row(&s, V, dO, b, h, i, dP);\n        double delta",
+    ("K row stride uses the query length", "return (((size_t)b * s->Tk + t) * s->HKV + g) * s->D;",
+     "return (((size_t)b * s->T + t) * s->HKV + g) * s->D;", 0),
+    ("scores over the query length", "for (long j = 0; j < s->Tk; ++j) {\n    if (visible(s, i, j))",
+     "for (long j = 0; j < s->T; ++j) {\n    if (visible(s, i, j))", 0),
+    ("probability rows strided by the query length", "double* row = P + (size_t)i * Tk;",
+     "double* row = P + (size_t)i * T;", 0),
+    ("dK/dV rows: Delta over the query length", "for (long j = 0; j < Tk; ++j) delta += P[j] * dP[j];",
+     "for (long j = 0; j < T; ++j) delta += P[j] * dP[j];", 1),
+    ("row LSE missing in dq rows", "softmax_row(P, Tk);\n        dp_row(&s, V, dO, b, h, i, dP);\n        double delta",
      "dp_row(&s, V, dO, b, h, i, dP);\n        double delta", 0),
 ]
 

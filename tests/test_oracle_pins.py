@@ -364,3 +364,132 @@ def test_triu_blocks_reproduce_printed_diagrams(name):
     assert np.array_equal(picture, diagram)
     # the masks the code adds cover exactly the strictly-upper (future) part
     assert np.array_equal(mask, np.triu(np.ones((n, n), np.int64), 1))
+
+
+# ------------------------------------------------ cross-attention (Tq != Tk)
+#
+# The teeny-kernels page (flash_attn2.rs, `flash_attention2_forward`) takes
+# separate query and key lengths and visits every key of every query row:
+# unmasked attention of Tq query rows over Tk key rows.
+
+CROSS = [
+    # B, Tq, Tk, H, HKV, D
+    (1, 3, 8, 2, 1, 4),
+    (2, 9, 4, 4, 2, 5),
+    (1, 1, 13, 3, 3, 3),
+    (1, 12, 1, 2, 2, 4),
+    (2, 6, 11, 6, 2, 6),
+]
+
+
+def rand_cross(rng, B, Tq, Tk, H, HKV, D):
+    Q = rng.standard_normal((B, Tq, H, D))
+    K = rng.standard_normal((B, Tk, HKV, D))
+    V = rng.standard_normal((B, Tk, HKV, D))
+    dO = rng.standard_normal((B, Tq, H, D))
+    return Q, K, V, dO
+
+
+@pytest.mark.parametrize("case", CROSS)
+def test_cross_attention_matches_torch_sdpa_and_autograd(case):
+    B, Tq, Tk, H, HKV, D = case
+    rng = np.random.default_rng(71 + Tq + Tk)
+    Q, K, V, dO = rand_cross(rng, B, Tq, Tk, H, HKV, D)
+    scale = 0.6
+    O, LSE = oracle.fwd(Q, K, V, scale, False, 0)
+    dQ, dK, dV, Delta = oracle.bwd(Q, K, V, dO, scale, False, 0)
+    assert O.shape == Q.shape and LSE.shape == (B, H, Tq) and dK.shape == K.shape and Delta.shape == (B, H, Tq)
+    q = torch.tensor(Q).permute(0, 2, 1, 3).requires_grad_(True)
+    k = torch.tensor(K).permute(0, 2, 1, 3).requires_grad_(True)
+    v = torch.tensor(V).permute(0, 2, 1, 3).requires_grad_(True)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale, enable_gqa=True)
+    o.backward(torch.tensor(dO).permute(0, 2, 1, 3))
+    np.testing.assert_allclose(O, o.detach().permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    for a, t in ((dQ, q), (dK, k), (dV, v)):
+        np.testing.assert_allclose(a, t.grad.permute(0, 2, 1, 3).numpy(), rtol=0, atol=1e-12)
+    rep = H // HKV
+    kk = torch.tensor(K).repeat_interleave(rep, dim=2)
+    S = scale * torch.einsum("bihd,bjhd->bhij", torch.tensor(Q), kk)
+    np.testing.assert_allclose(LSE, torch.logsumexp(S, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", CROSS[:3] + CROSS[4:])
+def test_cross_attention_key_split_merges_by_lse(case):
+    """Attention over keys [K1; K2] is the LSE-weighted merge of attention
+    over K1 and over K2: O = (e^L1 O1 + e^L2 O2) / (e^L1 + e^L2),
+    L = log(e^L1 + e^L2)."""
+    B, Tq, Tk, H, HKV, D = case
+    rng = np.random.default_rng(83 + Tk)
+    Q, K, V, _ = rand_cross(rng, B, Tq, Tk, H, HKV, D)
+    cut = Tk // 2
+    O, L = oracle.fwd(Q, K, V, 0.5, False, 0)
+    O1, L1 = oracle.fwd(Q, K[:, :cut], V[:, :cut], 0.5, False, 0)
+    O2, L2 = oracle.fwd(Q, K[:, cut:], V[:, cut:], 0.5, False, 0)
+    Lm = np.logaddexp(L1, L2)
+    w1 = np.exp(L1 - Lm).transpose(0, 2, 1)[..., None]
+    w2 = np.exp(L2 - Lm).transpose(0, 2, 1)[..., None]
+    np.testing.assert_allclose(L, Lm, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(O, w1 * O1 + w2 * O2, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", CROSS)
+def test_cross_attention_is_invariant_to_key_order(case):
+    """Permuting the key rows (K and V together) leaves O, LSE and dQ
+    unchanged and permutes dK and dV the same way."""
+    B, Tq, Tk, H, HKV, D = case
+    rng = np.random.default_rng(89 + Tq)
+    Q, K, V, dO = rand_cross(rng, B, Tq, Tk, H, HKV, D)
+    perm = rng.permutation(Tk)
+    O, L = oracle.fwd(Q, K, V, 0.7, False, 0)
+    Op, Lp = oracle.fwd(Q, K[:, perm], V[:, perm], 0.7, False, 0)
+    np.testing.assert_allclose(Op, O, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(Lp, L, rtol=0, atol=1e-12)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, 0.7, False, 0)
+    dQp, dKp, dVp, _ = oracle.bwd(Q, K[:, perm], V[:, perm], dO, 0.7, False, 0)
+    np.testing.assert_allclose(dQp, dQ, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dKp, dK[:, perm], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dVp, dV[:, perm], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("Tq,Tk,HKV", [(2, 5, 1), (4, 3, 2), (1, 4, 1)])
+def test_cross_attention_gradients_match_central_differences(Tq, Tk, HKV):
+    B, H, D = 1, 2, 2
+    rng = np.random.default_rng(97 + Tq * Tk)
+    Q, K, V, dO = rand_cross(rng, B, Tq, Tk, H, HKV, D)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, 0.9, False, 0)
+
+    def loss(q, k, v):
+        return float(np.sum(oracle.fwd(q, k, v, 0.9, False, 0)[0] * dO))
+
+    h = 1e-6
+    for X, G, which in ((Q, dQ, 0), (K, dK, 1), (V, dV, 2)):
+        for idx in np.ndindex(X.shape):
+            plus = [Q.copy(), K.copy(), V.copy()]
+            minus = [Q.copy(), K.copy(), V.copy()]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd = (loss(*plus) - loss(*minus)) / (2 * h)
+            assert abs(fd - G[idx]) <= 1e-7 * max(1.0, abs(G[idx])), (which, idx, fd, G[idx])
+
+
+@pytest.mark.parametrize("case", CROSS)
+def test_cross_attention_row_functions_agree_with_full_functions(case):
+    B, Tq, Tk, H, HKV, D = case
+    rng = np.random.default_rng(101)
+    Q, K, V, dO = rand_cross(rng, B, Tq, Tk, H, HKV, D)
+    O, LSE = oracle.fwd(Q, K, V, 0.5, False, 0)
+    dQ, dK, dV, Delta = oracle.bwd(Q, K, V, dO, 0.5, False, 0)
+    rows = sorted({0, Tq - 1, Tq // 2})
+    cols = sorted({0, Tk - 1, Tk // 2})
+    b = B - 1
+    for h in range(H):
+        o_r, l_r = oracle.fwd_rows(Q, K, V, 0.5, False, 0, b, h, rows)
+        np.testing.assert_allclose(o_r, O[b, rows, h], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l_r, LSE[b, h, rows], rtol=0, atol=1e-13)
+        dq_r, de_r = oracle.dq_rows(Q, K, V, dO, 0.5, False, 0, b, h, rows)
+        np.testing.assert_allclose(dq_r, dQ[b, rows, h], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(de_r, Delta[b, h, rows], rtol=0, atol=1e-13)
+    for g in range(HKV):
+        dk_r, dv_r = oracle.dkdv_rows(Q, K, V, dO, 0.5, False, 0, b, g, cols)
+        np.testing.assert_allclose(dk_r, dK[b, cols, g], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(dv_r, dV[b, cols, g], rtol=0, atol=1e-12)
