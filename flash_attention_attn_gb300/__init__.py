@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     attention_fwd,
     check_status,
     fa_bwd,
+    fa_bwd_cross,
     fa_bwd_dkdv,
     fa_bwd_dq,
     fa_bwd_preprocess,
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     fa_debug_config,
     fa_debug_fwd_tiles,
     fa_fwd,
+    fa_fwd_cross,
     fa_plan_block_mask,
     fa_plan_kv_range,
     fa_plan_q_range,

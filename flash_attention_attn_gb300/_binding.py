@@ -68,6 +68,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_fwd.restype = _i
         lib.fa_bwd.argtypes = [_vp] * 9 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd.restype = _i
+        lib.fa_fwd_cross.argtypes = [_vp] * 5 + [_i] * 6 + [_f, _i, _vp, _sz, _vp]
+        lib.fa_fwd_cross.restype = _i
+        lib.fa_bwd_cross.argtypes = [_vp] * 9 + [_i] * 6 + [_f, _i, _vp, _sz, _vp]
+        lib.fa_bwd_cross.restype = _i
         lib.fa_bwd_preprocess.argtypes = [_vp, _vp] + [_i] * 6 + [_vp, _sz, _vp]
         lib.fa_bwd_preprocess.restype = _i
         lib.fa_bwd_dkdv.argtypes = [_vp] * 7 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
@@ -115,6 +119,18 @@ def fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causa
            workspace, workspace_bytes, stream) -> int:
     return load().fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal,
                          window, dtype, workspace, workspace_bytes, stream)
+
+
+def fa_fwd_cross(Q, K, V, O, LSE, B, Tq, Tk, H, HKV, head_dim, scale, dtype, workspace, workspace_bytes,
+                 stream) -> int:
+    return load().fa_fwd_cross(Q, K, V, O, LSE, B, Tq, Tk, H, HKV, head_dim, scale, dtype, workspace,
+                               workspace_bytes, stream)
+
+
+def fa_bwd_cross(Q, K, V, O, LSE, dO, dQ, dK, dV, B, Tq, Tk, H, HKV, head_dim, scale, dtype, workspace,
+                 workspace_bytes, stream) -> int:
+    return load().fa_bwd_cross(Q, K, V, O, LSE, dO, dQ, dK, dV, B, Tq, Tk, H, HKV, head_dim, scale, dtype,
+                               workspace, workspace_bytes, stream)
 
 
 def fa_bwd_preprocess(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream) -> int:
@@ -246,14 +262,19 @@ def _stream(device, stream):
 
 
 def attention_fwd(q, k, v, scale=None, causal=True, window=0, out=None, lse=None, stream=None):
-    """O [B,T,H,D] and LSE [B,H,T] (fp32) for q [B,T,H,D], k/v [B,T,HKV,D]."""
+    """O [B,T,H,D] and LSE [B,H,T] (fp32) for q [B,T,H,D], k/v [B,Tk,HKV,D].
+
+    Tk != T (cross-attention) runs fa_fwd_cross: unmasked attention only, so
+    causal and window must then be off."""
     torch = _torch()
     B, T, H, D = q.shape
-    HKV = k.shape[2]
+    Tk, HKV = k.shape[1], k.shape[2]
     dev = q.device
     dt = _dtype_code(q)
-    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, T, HKV, D)), ("v", v, (B, T, HKV, D))):
+    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, Tk, HKV, D)), ("v", v, (B, Tk, HKV, D))):
         _check_tensor(name, t, shp, q.dtype, dev)
+    if Tk != T and (causal or window):
+        raise FaError(FA_ERR_UNSUPPORTED, "attention_fwd: causal or window masking needs len(k) == len(q)")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q) if out is None else out
@@ -262,6 +283,12 @@ def attention_fwd(q, k, v, scale=None, causal=True, window=0, out=None, lse=None
     _check_tensor("lse", l, (B, H, T), torch.float32, dev)
     s = _stream(dev, stream)
     ws, n = workspace(FA_OP_FWD, B, T, H, HKV, D, dt, dev, s)
+    if Tk != T:
+        st = fa_fwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, T, Tk, H, HKV,
+                          D, float(scale), dt, ws.data_ptr(), n, s)
+        if st != FA_OK:
+            raise FaError(st, "fa_fwd_cross")
+        return o, l
     st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(), B, T, H, HKV, D,
                 float(scale), int(bool(causal)), int(window), dt, ws.data_ptr(), n, s)
     if st != FA_OK:
@@ -271,16 +298,19 @@ def attention_fwd(q, k, v, scale=None, causal=True, window=0, out=None, lse=None
 
 def attention_bwd(q, k, v, o, lse, do, scale=None, causal=True, window=0, dq=None, dk=None, dv=None,
                   stream=None):
-    """dQ, dK, dV given the forward's O and LSE and the output gradient dO."""
+    """dQ, dK, dV given the forward's O and LSE and the output gradient dO
+    (cross-attention when k and v are longer or shorter than q)."""
     torch = _torch()
     B, T, H, D = q.shape
-    HKV = k.shape[2]
+    Tk, HKV = k.shape[1], k.shape[2]
     dev = q.device
     dt = _dtype_code(q)
-    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, T, HKV, D)), ("v", v, (B, T, HKV, D)),
+    for name, t, shp in (("q", q, (B, T, H, D)), ("k", k, (B, Tk, HKV, D)), ("v", v, (B, Tk, HKV, D)),
                          ("o", o, (B, T, H, D)), ("do", do, (B, T, H, D))):
         _check_tensor(name, t, shp, q.dtype, dev)
     _check_tensor("lse", lse, (B, H, T), torch.float32, dev)
+    if Tk != T and (causal or window):
+        raise FaError(FA_ERR_UNSUPPORTED, "attention_bwd: causal or window masking needs len(k) == len(q)")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
@@ -288,6 +318,13 @@ def attention_bwd(q, k, v, o, lse, do, scale=None, causal=True, window=0, dq=Non
     dv = torch.empty_like(v) if dv is None else dv
     s = _stream(dev, stream)
     ws, n = workspace(FA_OP_BWD, B, T, H, HKV, D, dt, dev, s)
+    if Tk != T:
+        st = fa_bwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, T, Tk, H, HKV, D, float(scale), dt,
+                          ws.data_ptr(), n, s)
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_cross")
+        return dq, dk, dv
     st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, T, H, HKV, D, float(scale),
                 int(bool(causal)), int(window), dt, ws.data_ptr(), n, s)

@@ -26,10 +26,14 @@ std::atomic<int> g_fwd_tiles{0};  // 0 = automatic
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int validate_shape(int B, int T, int H, int HKV, int D, float scale, int causal, int window, int dtype) {
-  if (B < 1 || T < 1 || H < 1 || HKV < 1 || D < 1) return FA_ERR_INVALID_ARG;
+// T: query rows, Tk: key rows (T for self-attention).
+int validate_shape(int B, int T, int Tk, int H, int HKV, int D, float scale, int causal, int window, int dtype) {
+  if (B < 1 || T < 1 || Tk < 1 || H < 1 || HKV < 1 || D < 1) return FA_ERR_INVALID_ARG;
   if (H % HKV != 0) return FA_ERR_INVALID_ARG;
   if (window < 0 || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
+  // queries and keys of different lengths: unmasked attention only (the
+  // pages place no causal diagonal or window between two sequences)
+  if (Tk != T && (causal || window)) return FA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || scale == INFINITY) return FA_ERR_INVALID_ARG;  // also rejects NaN
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP32 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_FP32) {
@@ -42,7 +46,8 @@ int validate_shape(int B, int T, int H, int HKV, int D, float scale, int causal,
   // grid limits (y = heads, z = batch) and 32-bit row indexing inside kernels
   if (H > 65535 || B > 65535) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * T * H * D >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(T) + window >= (1ll << 30)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Tk * HKV * D >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(T) + window >= (1ll << 30) || Tk >= (1 << 30)) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
 
@@ -124,16 +129,20 @@ bool fwd_two_tiles(const Shape& s) {
 extern "C" {
 
 size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype) {
-  if (validate_shape(B, T, H, HKV, head_dim, 1.f, 1, 0, dtype) != FA_OK) return 0;
+  if (validate_shape(B, T, T, H, HKV, head_dim, 1.f, 1, 0, dtype) != FA_OK) return 0;
   if (op == FA_OP_FWD) return kErrBytes;
   if (op == FA_OP_BWD) return kErrBytes + delta_bytes(B, T, H);
   return 0;
 }
 
-int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int T, int H, int HKV,
-           int head_dim, float scale, int causal, int window, int dtype, void* workspace, size_t workspace_bytes,
-           void* stream) {
-  int st = validate_shape(B, T, H, HKV, head_dim, scale, causal, window, dtype);
+}  // extern "C"
+
+namespace {
+
+int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int T, int Tk, int H, int HKV,
+             int head_dim, float scale, int causal, int window, int dtype, void* workspace, size_t workspace_bytes,
+             void* stream) {
+  int st = validate_shape(B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype);
   if (st != FA_OK) return st;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(LSE)) return FA_ERR_INVALID_ARG;
@@ -143,15 +152,15 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   int dev;
   if ((st = device_ok(&dev)) != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const Shape shp{B, T, H, HKV, head_dim, scale, causal, window};
+  const Shape shp{B, T, H, HKV, head_dim, scale, causal, window, Tk};
   if (dtype == FA_DTYPE_FP32)
     return status_of(fa::launch_fwd_fp32(static_cast<const float*>(Q), static_cast<const float*>(K),
                                          static_cast<const float*>(V), static_cast<float*>(O), LSE, shp, s));
   if ((st = get_encoder()) != FA_OK) return st;
   fa::TensorMaps tm;
   if ((st = encode_map(&tm.q, Q, B, T, H, head_dim, dtype)) != FA_OK) return st;
-  if ((st = encode_map(&tm.k, K, B, T, HKV, head_dim, dtype)) != FA_OK) return st;
-  if ((st = encode_map(&tm.v, V, B, T, HKV, head_dim, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm.k, K, B, Tk, HKV, head_dim, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm.v, V, B, Tk, HKV, head_dim, dtype)) != FA_OK) return st;
   fa::FwdParams p;
   p.s = shp;
   p.O = O;
@@ -164,13 +173,11 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   return status_of(fa::launch_fwd_bf16(tm, p, s));
 }
 
-namespace {
-
 // Shared checks of the backward stages; fills the shape and the Delta pointer.
-int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int H, int HKV, int head_dim, float scale,
+int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int Tk, int H, int HKV, int head_dim, float scale,
                  int causal, int window, int dtype, void* workspace, size_t workspace_bytes, Shape* shp,
                  float** delta) {
-  int st = validate_shape(B, T, H, HKV, head_dim, scale, causal, window, dtype);
+  int st = validate_shape(B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype);
   if (st != FA_OK) return st;
   for (int i = 0; i < nptr; ++i)
     if (!ptrs[i] || !aligned16(ptrs[i])) return FA_ERR_INVALID_ARG;
@@ -179,7 +186,7 @@ int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int H, int HKV
     return FA_ERR_WORKSPACE;
   int dev;
   if ((st = device_ok(&dev)) != FA_OK) return st;
-  *shp = Shape{B, T, H, HKV, head_dim, scale, causal, window};
+  *shp = Shape{B, T, H, HKV, head_dim, scale, causal, window, Tk};
   *delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + kErrBytes);
   return FA_OK;
 }
@@ -189,8 +196,8 @@ int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, co
   int st;
   if ((st = get_encoder()) != FA_OK) return st;
   if ((st = encode_map(&tm->q, Q, s.B, s.T, s.H, s.D, dtype)) != FA_OK) return st;
-  if ((st = encode_map(&tm->k, K, s.B, s.T, s.HKV, s.D, dtype)) != FA_OK) return st;
-  if ((st = encode_map(&tm->v, V, s.B, s.T, s.HKV, s.D, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm->k, K, s.B, s.Tk, s.HKV, s.D, dtype)) != FA_OK) return st;
+  if ((st = encode_map(&tm->v, V, s.B, s.Tk, s.HKV, s.D, dtype)) != FA_OK) return st;
   if ((st = encode_map(&tm->dO, dO, s.B, s.T, s.H, s.D, dtype)) != FA_OK) return st;
   return FA_OK;
 }
@@ -211,26 +218,25 @@ fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, v
   return p;
 }
 
-}  // namespace
-
-int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
-                      void* workspace, size_t workspace_bytes, void* stream) {
+int preprocess_impl(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
   const void* ptrs[] = {O, dO};
   Shape shp;
   float* delta;
-  int st = bwd_prologue(ptrs, 2, B, T, H, HKV, head_dim, 1.f, 1, 0, dtype, workspace, workspace_bytes, &shp, &delta);
+  int st = bwd_prologue(ptrs, 2, B, T, T, H, HKV, head_dim, 1.f, 1, 0, dtype, workspace, workspace_bytes, &shp,
+                        &delta);
   if (st != FA_OK) return st;
   return status_of(fa::launch_delta(O, dO, delta, shp, dtype, static_cast<cudaStream_t>(stream)));
 }
 
-int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
-                int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
-                void* workspace, size_t workspace_bytes, void* stream) {
+int dkdv_impl(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
+              int B, int T, int Tk, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+              void* workspace, size_t workspace_bytes, void* stream) {
   const void* ptrs[] = {Q, K, V, LSE, dO, dK, dV};
   Shape shp;
   float* delta;
-  int st = bwd_prologue(ptrs, 7, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
-                        &shp, &delta);
+  int st = bwd_prologue(ptrs, 7, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                        workspace_bytes, &shp, &delta);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == FA_DTYPE_FP32)
@@ -242,14 +248,14 @@ int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, c
   return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace, dtype), s));
 }
 
-int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
-              int H, int HKV, int head_dim, float scale, int causal, int window, int dtype, void* workspace,
-              size_t workspace_bytes, void* stream) {
+int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
+            int Tk, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype, void* workspace,
+            size_t workspace_bytes, void* stream) {
   const void* ptrs[] = {Q, K, V, LSE, dO, dQ};
   Shape shp;
   float* delta;
-  int st = bwd_prologue(ptrs, 6, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
-                        &shp, &delta);
+  int st = bwd_prologue(ptrs, 6, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                        workspace_bytes, &shp, &delta);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == FA_DTYPE_FP32)
@@ -261,24 +267,75 @@ int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, con
   return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype), s));
 }
 
-int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
-           void* dK, void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
-           int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+             void* dK, void* dV, int B, int T, int Tk, int H, int HKV, int head_dim, float scale, int causal,
+             int window, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
   // validate every argument before the first launch, so that a bad call
   // launches nothing
   const void* ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
   Shape shp;
   float* delta;
-  int st = bwd_prologue(ptrs, 9, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
-                        &shp, &delta);
+  int st = bwd_prologue(ptrs, 9, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                        workspace_bytes, &shp, &delta);
   if (st != FA_OK) return st;
-  if ((st = fa_bwd_preprocess(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)) != FA_OK)
+  if ((st = preprocess_impl(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
-  if ((st = fa_bwd_dkdv(Q, K, V, LSE, dO, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
-                        workspace_bytes, stream)) != FA_OK)
+  if ((st = dkdv_impl(Q, K, V, LSE, dO, dK, dV, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                      workspace_bytes, stream)) != FA_OK)
     return st;
-  return fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+  return dq_impl(Q, K, V, LSE, dO, dQ, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                 workspace_bytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int T, int H, int HKV,
+           int head_dim, float scale, int causal, int window, int dtype, void* workspace, size_t workspace_bytes,
+           void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                  workspace_bytes, stream);
+}
+
+int fa_fwd_cross(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Tq, int Tk, int H,
+                 int HKV, int head_dim, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, Tq, Tk, H, HKV, head_dim, scale, 0, 0, dtype, workspace, workspace_bytes,
+                  stream);
+}
+
+int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  return preprocess_impl(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dK, void* dV,
+                int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  return dkdv_impl(Q, K, V, LSE, dO, dK, dV, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
                    workspace_bytes, stream);
+}
+
+int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
+              int H, int HKV, int head_dim, float scale, int causal, int window, int dtype, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  return dq_impl(Q, K, V, LSE, dO, dQ, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                 workspace_bytes, stream);
+}
+
+int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
+           void* dK, void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window,
+           int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, T, H, HKV, head_dim, scale, causal, window, dtype,
+                  workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_cross(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                 void* dQ, void* dK, void* dV, int B, int Tq, int Tk, int H, int HKV, int head_dim, float scale,
+                 int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(Q, K, V, O, LSE, dO, dQ, dK, dV, B, Tq, Tk, H, HKV, head_dim, scale, 0, 0, dtype, workspace,
+                  workspace_bytes, stream);
 }
 
 int fa_check_status(void* workspace, void* stream, unsigned int* raw_word) {
@@ -311,20 +368,20 @@ const char* fa_status_string(int status) {
 int fa_plan_kv_range(int T, int BM, int BN, int causal, int window, int qb, int* lo, int* hi) {
   if (T < 1 || BM < 1 || BN < 1 || window < 0 || !lo || !hi || qb < 0 || qb >= fa::ceil_div(T, BM))
     return FA_ERR_INVALID_ARG;
-  fa::kv_range_for_q(T, BM, BN, causal, window, qb, *lo, *hi);
+  fa::kv_range_for_q(T, T, BM, BN, causal, window, qb, *lo, *hi);
   return FA_OK;
 }
 
 int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* lo, int* hi) {
   if (T < 1 || BM < 1 || BN < 1 || window < 0 || !lo || !hi || kb < 0 || kb >= fa::ceil_div(T, BN))
     return FA_ERR_INVALID_ARG;
-  fa::q_range_for_kv(T, BM, BN, causal, window, kb, *lo, *hi);
+  fa::q_range_for_kv(T, T, BM, BN, causal, window, kb, *lo, *hi);
   return FA_OK;
 }
 
 int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb) {
   if (T < 1 || BM < 1 || BN < 1 || window < 0 || qb < 0 || kb < 0) return -FA_ERR_INVALID_ARG;
-  return fa::block_needs_mask(T, BM, BN, causal, window, qb, kb) ? 1 : 0;
+  return fa::block_needs_mask(T, T, BM, BN, causal, window, qb, kb) ? 1 : 0;
 }
 
 int fa_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens, int hq,

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int rep = s.H / s.HKV;
   int qlo, qhi;
-  q_range_for_kv(s.T, BQ, BK, s.causal, s.window, kb, qlo, qhi);
+  q_range_for_kv(s.T, s.Tk, BQ, BK, s.causal, s.window, kb, qlo, qhi);
   const int nqb = qhi - qlo + 1;
   const int niter = rep * nqb;  // (head r, query block qb) pairs, r outer
 
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait(&bars->s_full[0], n & 1, ctl, kCode))) break;
       if (!(ok = warp_wait(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode))) break;  // rows visible
       tc_fence_after();
-      const bool need_mask = block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb);
+      const bool need_mask = block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb);
       float pv[64];
       {
         float lo[32], hi[32];
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (need_mask) {
         const int i0 = qb * BQ + half * 64;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
+        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.Tk, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
       }
       {
         uint32_t pk[32];
@@ -428,12 +428,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
     if (ok) {
       tc_fence_after();
-      const size_t rowoff = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * s.D + half * (D / 2);
+      const size_t rowoff = ((static_cast<size_t>(b) * s.Tk + j) * s.HKV + g) * s.D + half * (D / 2);
       const int nvalid = s.D - half * (D / 2);  // columns of this half inside the head dim
       store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, nvalid, 1.f,
-                         static_cast<uint16_t*>(p.dV) + rowoff, j < s.T);
+                         static_cast<uint16_t*>(p.dV) + rowoff, j < s.Tk);
       store_acc_row<F16>(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, nvalid, s.scale,
-                         static_cast<uint16_t*>(p.dK) + rowoff, j < s.T);
+                         static_cast<uint16_t*>(p.dK) + rowoff, j < s.Tk);
     }
   }
 
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int g = h / (s.H / s.HKV);
   int kb_lo, kb_hi;
-  kv_range_for_q(s.T, BQ, BK, s.causal, s.window, qb, kb_lo, kb_hi);
+  kv_range_for_q(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb_lo, kb_hi);
   const int nblk = kb_hi - kb_lo + 1;
 
   if (threadIdx.x == 0) init_bars(bars, 1);
@@ -635,10 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           pv[33 + c] = ex2(y1);
         }
       }
-      if (block_needs_mask(s.T, BQ, BK, s.causal, s.window, qb, kb)) {
+      if (block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb)) {
         const int j0 = kb * BK + half * 64;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.Tk, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
       }
       // pass 2: dS = P (dP - Delta) -> bf16 over the S columns this thread read
       if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
@@ -691,7 +691,7 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(p.s.T, 128), p.s.HKV, p.s.B);
+  dim3 grid(ceil_div(p.s.Tk, 128), p.s.HKV, p.s.B);
   fa_bwd_dkdv_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }

@@ -30,7 +30,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ void visible_keys(const Shape& s, int i, int& jlo, int& jhi) {
   jlo = (s.window > 0) ? max(0, i - s.window + 1) : 0;
-  jhi = s.causal ? i : s.T - 1;
+  jhi = s.causal ? min(i, s.Tk - 1) : s.Tk - 1;
 }
 
 __device__ __forceinline__ void visible_queries(const Shape& s, int j, int& ilo, int& ihi) {
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kWarps * 32) fa_fwd_fp32_kernel(const float* _
   int jlo, jhi;
   visible_keys(s, i, jlo, jhi);
   for (int j = jlo; j <= jhi; ++j) {
-    const size_t kv = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D;
+    const size_t kv = ((static_cast<size_t>(b) * s.Tk + j) * s.HKV + g) * D;
     float part = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) part = fmaf(q[e], K[kv + lane + 32 * e], part);
@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(kWarps * 32) fa_bwd_dq_fp32_kernel(const float
   int jlo, jhi;
   visible_keys(s, i, jlo, jhi);
   for (int j = jlo; j <= jhi; ++j) {
-    const size_t kv = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D;
+    const size_t kv = ((static_cast<size_t>(b) * s.Tk + j) * s.HKV + g) * D;
     float ps = 0.f, pd = 0.f;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
@@ -131,9 +131,9 @@ __global__ void __launch_bounds__(kWarps * 32) fa_bwd_dkdv_fp32_kernel(const flo
   const int lane = threadIdx.x & 31;
   const int j = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int g = blockIdx.y, b = blockIdx.z;
-  if (j >= s.T) return;
+  if (j >= s.Tk) return;
   const int rep = s.H / s.HKV;
-  const size_t kvo = ((static_cast<size_t>(b) * s.T + j) * s.HKV + g) * D;
+  const size_t kvo = ((static_cast<size_t>(b) * s.Tk + j) * s.HKV + g) * D;
   float k[E], v[E], dk[E], dv[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
@@ -184,7 +184,7 @@ cudaError_t fwd_d(const float* Q, const float* K, const float* V, float* O, floa
 template <int D>
 cudaError_t dkdv_d(const float* Q, const float* K, const float* V, const float* dO, const float* LSE,
                    const float* Delta, float* dK, float* dV, const Shape& s, cudaStream_t st) {
-  dim3 grid(ceil_div(s.T, kWarps), s.HKV, s.B);
+  dim3 grid(ceil_div(s.Tk, kWarps), s.HKV, s.B);
   fa_bwd_dkdv_fp32_kernel<D><<<grid, kWarps * 32, 0, st>>>(Q, K, V, dO, LSE, Delta, dK, dV, s);
   return cudaGetLastError();
 }

@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int g = h / (s.H / s.HKV);
   int kb_lo, kb_hi;
-  kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, qb, kb_lo, kb_hi);
+  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, qb, kb_lo, kb_hi);
   const int nblk = kb_hi - kb_lo + 1;
 
   if (threadIdx.x == 0) {
@@ -257,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         sv[64 + c] = __uint_as_float(r2[c]);
         sv[96 + c] = __uint_as_float(r3[c]);
       }
-      if (block_needs_mask(s.T, kBM, kBN, s.causal, s.window, qb, kb)) {
+      if (block_needs_mask(s.T, s.Tk, kBM, kBN, s.causal, s.window, qb, kb)) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (masked(s.T, s.causal, s.window, row, kb * kBN + c)) sv[c] = -CUDART_INF_F;
+          if (masked(s.T, s.Tk, s.causal, s.window, row, kb * kBN + c)) sv[c] = -CUDART_INF_F;
       }
       float mx = sv[0];
 #pragma unroll
@@ -432,8 +432,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int g = h / (s.H / s.HKV);
   // visible KV block range of each tile (B is empty past the end)
   int lo_a, hi_a, lo_b = 1, hi_b = 0;
-  kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, 2 * pair, lo_a, hi_a);
-  if (2 * pair + 1 < nq) kv_range_for_q(s.T, kBM, kBN, s.causal, s.window, 2 * pair + 1, lo_b, hi_b);
+  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, 2 * pair, lo_a, hi_a);
+  if (2 * pair + 1 < nq) kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, 2 * pair + 1, lo_b, hi_b);
   const bool has_b = lo_b <= hi_b;
   const int lo = has_b ? imin(lo_a, lo_b) : lo_a;
   const int hi = has_b ? imax(hi_a, hi_b) : hi_a;
@@ -598,7 +598,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // The masking pre-pass stays rolled over 32-column chunks: unrolled with
       // everything else, this softmax did not fit the instruction cache next
       // to the other roles and ran several times slower.
-      if (block_needs_mask(s.T, kBM, kBN, s.causal, s.window, q, kb)) {
+      if (block_needs_mask(s.T, s.Tk, kBM, kBN, s.causal, s.window, q, kb)) {
         // rare (diagonal, window-edge and tail blocks): -inf over the masked
         // scores in TMEM, so that both passes below stay mask-free
 #pragma unroll 1
@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
           tmem_ld_wait(ra);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (masked(s.T, s.causal, s.window, row, kb * kBN + c4 * 32 + c)) ra[c] = __float_as_uint(-CUDART_INF_F);
+            if (masked(s.T, s.Tk, s.causal, s.window, row, kb * kBN + c4 * 32 + c)) ra[c] = __float_as_uint(-CUDART_INF_F);
           tmem_st32(s_addr + c4 * 32, ra);
         }
         tmem_st_wait();

@@ -19,49 +19,52 @@ __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : 
 __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 
 // Visible(i, j) = (!causal || j <= i) && (window == 0 || i - j < window),
-// and both indices inside the sequence.
-__host__ __device__ __forceinline__ bool masked(int T, int causal, int window, int i, int j) {
-  return i >= T || j >= T || (causal && j > i) || (window > 0 && i - j >= window);
+// with query row i < Tq and key row j < Tk (Tq = Tk for self-attention; the
+// library accepts Tq != Tk only without causal or window masking).
+__host__ __device__ __forceinline__ bool masked(int Tq, int Tk, int causal, int window, int i, int j) {
+  return i >= Tq || j >= Tk || (causal && j > i) || (window > 0 && i - j >= window);
 }
 
 // KV blocks [lo, hi] that query tile qb must visit: blocks wholly above the
 // causal diagonal or wholly before the window are skipped.
-__host__ __device__ __forceinline__ void kv_range_for_q(int T, int BM, int BN, int causal, int window,
+__host__ __device__ __forceinline__ void kv_range_for_q(int Tq, int Tk, int BM, int BN, int causal, int window,
                                                         int qb, int& lo, int& hi) {
-  const int nkv = ceil_div(T, BN);
+  const int nkv = ceil_div(Tk, BN);
   const int row_lo = qb * BM;
-  const int row_hi = imin(qb * BM + BM - 1, T - 1);
+  const int row_hi = imin(qb * BM + BM - 1, Tq - 1);
   hi = causal ? imin(nkv - 1, row_hi / BN) : nkv - 1;
   lo = window > 0 ? imax(0, row_lo - window + 1) / BN : 0;
 }
 
 // Query tiles [lo, hi] that see any key of KV block kb.
-__host__ __device__ __forceinline__ void q_range_for_kv(int T, int BM, int BN, int causal, int window,
+__host__ __device__ __forceinline__ void q_range_for_kv(int Tq, int Tk, int BM, int BN, int causal, int window,
                                                         int kb, int& lo, int& hi) {
-  const int nq = ceil_div(T, BM);
+  const int nq = ceil_div(Tq, BM);
   const int col_lo = kb * BN;
-  const int col_hi = imin(kb * BN + BN - 1, T - 1);
+  const int col_hi = imin(kb * BN + BN - 1, Tk - 1);
   lo = causal ? col_lo / BM : 0;
   hi = window > 0 ? imin(nq - 1, (col_hi + window - 1) / BM) : nq - 1;
 }
 
-// Does block (qb, kb) hold any masked element (including indices >= T)?
-// Under causal masking with BM = BN these are the diagonal blocks: the
-// block-offset k = qb*BM - kb*BN + 1 is the triu offset of that block.
-__host__ __device__ __forceinline__ bool block_needs_mask(int T, int BM, int BN, int causal, int window,
+// Does block (qb, kb) hold any masked element (including rows >= Tq and
+// keys >= Tk)?  Under causal masking with BM = BN these are the diagonal
+// blocks: the block-offset k = qb*BM - kb*BN + 1 is the triu offset of that
+// block.
+__host__ __device__ __forceinline__ bool block_needs_mask(int Tq, int Tk, int BM, int BN, int causal, int window,
                                                           int qb, int kb) {
   const int row_lo = qb * BM, row_hi = qb * BM + BM - 1;
   const int col_lo = kb * BN, col_hi = kb * BN + BN - 1;
-  if (row_hi >= T || col_hi >= T) return true;
+  if (row_hi >= Tq || col_hi >= Tk) return true;
   if (causal && col_hi > row_lo) return true;
   if (window > 0 && row_hi - col_lo >= window) return true;
   return false;
 }
 
 struct Shape {
-  int B, T, H, HKV, D;
+  int B, T, H, HKV, D;  // T: query rows
   float scale;
   int causal, window;
+  int Tk;  // key rows (T for self-attention)
 };
 
 // ------------------------------------------------------------ bf16 kernels

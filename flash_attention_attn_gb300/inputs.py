@@ -88,6 +88,17 @@ def make_inputs(w: Workload, seed: int | None = None, with_dO: bool = True) -> d
     return out
 
 
+def make_cross_inputs(dtype: str, B: int, H: int, HKV: int, Tq: int, Tk: int, D: int,
+                      seed: int) -> dict[str, torch.Tensor]:
+    """Cross-attention inputs: q, do [B,Tq,H,D] and k, v [B,Tk,HKV,D], iid
+    N(0, 1) drawn in the order q, k, v, do, then cast to `dtype`."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shapes = {"q": (B, Tq, H, D), "k": (B, Tk, HKV, D), "v": (B, Tk, HKV, D), "do": (B, Tq, H, D)}
+    dt = torch_dtype(dtype)
+    return {n: torch.randn(sh, generator=g, dtype=torch.float32).to(dt).contiguous() for n, sh in shapes.items()}
+
+
 def as_f64(t: torch.Tensor):
     """Exact widening of a CPU tensor to a float64 numpy array."""
     return t.detach().to("cpu").to(torch.float64).numpy()

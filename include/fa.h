@@ -56,10 +56,17 @@
  *
  * Supported: dtype FA_DTYPE_BF16 or FA_DTYPE_FP16 (tcgen05 tensor-core
  * kernels, fp32 accumulation; P and dS are rounded to the input type before
- * their MMAs) or FA_DTYPE_FP32 (fp32 CUDA-core kernels); head_dim 64 or
- * 128; any B, T, H, HKV >= 1 with H % HKV == 0; scale > 0 and finite;
- * window >= 0; 16-byte aligned tensor pointers.  No fallback path exists: an
- * unsupported shape is an error.
+ * their MMAs; head_dim 16 to 128 in steps of 8) or FA_DTYPE_FP32 (fp32
+ * CUDA-core kernels; head_dim 64 or 128); any B, T, H, HKV >= 1 with
+ * H % HKV == 0; scale > 0 and finite; window >= 0; 16-byte aligned tensor
+ * pointers.  No fallback path exists: an unsupported shape is an error.
+ *
+ * Cross-attention (fa_fwd_cross, fa_bwd_cross): Tq query rows attend to Tk
+ * key rows, Tk != Tq allowed, K/V/dK/dV then [B, Tk, HKV, head_dim] and
+ * Q/O/dO/dQ/LSE sized by Tq.  Every key is visible to every query (the
+ * teeny-kernels page's flash_attn2.rs forward takes n_ctx_q and n_ctx_k and
+ * masks nothing); causal and window masking are defined here only for
+ * Tq == Tk (fa_fwd, fa_bwd).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -131,6 +138,23 @@ int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, c
 int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ,
               int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Cross-attention: fa_fwd / fa_bwd for Tq query rows over Tk key rows, no
+ * mask (see the top of this file).
+ *   Q, O, dO, dQ [B,Tq,H,D]; K, V, dK, dV [B,Tk,HKV,D]; LSE [B,H,Tq] fp32.
+ *   Workspace: fa_workspace_size(op, B, Tq, H, HKV, head_dim, dtype) bytes
+ *   (Delta has one row per query).  Tq = Tk gives exactly fa_fwd / fa_bwd
+ *   with causal = 0, window = 0.  Same kernels, same errors and stream
+ *   behaviour as fa_fwd / fa_bwd; Tq or Tk < 1 is FA_ERR_INVALID_ARG.
+ */
+int fa_fwd_cross(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int Tq, int Tk, int H, int HKV, int head_dim, float scale,
+                 int dtype, void* workspace, size_t workspace_bytes, void* stream);
+int fa_bwd_cross(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
+                 const void* dO, void* dQ, void* dK, void* dV,
+                 int B, int Tq, int Tk, int H, int HKV, int head_dim, float scale,
+                 int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fa_bwd_static_scratch: fa_bwd for callers that cannot allocate device

@@ -97,12 +97,46 @@ def test_bwd_validation(lib):
     assert fb.fa_bwd(*p, *args, FAKE, 1 << 20, None) == fb.FA_ERR_INVALID_ARG
 
 
+def call_fwd_cross(B=1, Tq=100, Tk=300, H=2, HKV=1, D=64, scale=0.125, dtype=fb.FA_DTYPE_BF16, ptrs=None,
+                   ws=FAKE, ws_bytes=1 << 20):
+    p = ptrs or [FAKE] * 5
+    return fb.fa_fwd_cross(*p, B, Tq, Tk, H, HKV, D, scale, dtype, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Tq=0), fb.FA_ERR_INVALID_ARG),
+    (dict(Tk=0), fb.FA_ERR_INVALID_ARG),
+    (dict(H=3, HKV=2), fb.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fb.FA_ERR_INVALID_ARG),
+    (dict(D=100), fb.FA_ERR_UNSUPPORTED),
+    (dict(D=96, dtype=fb.FA_DTYPE_FP32), fb.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fb.FA_ERR_UNSUPPORTED),
+    (dict(ptrs=[FAKE, FAKE, 0, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
+    (dict(ptrs=[FAKE, FAKE + 8, FAKE, FAKE, FAKE]), fb.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fb.FA_ERR_WORKSPACE),
+    (dict(ws_bytes=16), fb.FA_ERR_WORKSPACE),
+])
+def test_fwd_cross_validation(lib, kw, code):
+    assert call_fwd_cross(**kw) == code
+
+
+def test_bwd_cross_validation(lib):
+    p = [FAKE] * 9
+    args = (1, 100, 300, 2, 1, 64, 0.125, fb.FA_DTYPE_BF16)
+    assert fb.fa_bwd_cross(*p, *args, FAKE, 256, None) == fb.FA_ERR_WORKSPACE  # needs room for Delta (Tq rows)
+    assert fb.fa_bwd_cross(*p, 1, 100, 0, 2, 1, 64, 0.125, fb.FA_DTYPE_BF16, FAKE, 1 << 20, None) == \
+        fb.FA_ERR_INVALID_ARG
+    p[7] = 0
+    assert fb.fa_bwd_cross(*p, *args, FAKE, 1 << 20, None) == fb.FA_ERR_INVALID_ARG
+
+
 def test_no_gpu_means_error_not_fallback(lib):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     st = call_fwd()
     assert st in (fb.FA_ERR_CUDA, fb.FA_ERR_UNSUPPORTED)
+    assert call_fwd_cross() in (fb.FA_ERR_CUDA, fb.FA_ERR_UNSUPPORTED)
 
 
 def test_forward_tiles_hook_validates(lib):

@@ -19,7 +19,7 @@ import torch
 
 import oracle
 import flash_attention_attn_gb300 as fa
-from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, as_f64, make_inputs
+from flash_attention_attn_gb300.inputs import WORKLOADS, Workload, as_f64, make_cross_inputs, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -193,6 +193,53 @@ def test_random_shapes_elementwise(case):
     check_grad(w, "dQ", got["dq"], dQ)
     check_grad(w, "dK", got["dk"], dK)
     check_grad(w, "dV", got["dv"], dV)
+
+
+# ------------------------------------------------ cross-attention (Tq != Tk)
+
+CROSS_CASES = [
+    # dtype, B, H, HKV, Tq, Tk, D
+    ("bf16", 2, 4, 2, 300, 77, 64),      # fewer keys than one block, ragged queries
+    ("bf16", 1, 8, 2, 129, 513, 128),    # two-tile forward, five key blocks with a tail
+    ("bf16", 1, 4, 1, 700, 128, 128),    # many query tiles over one exact key block
+    ("fp16", 1, 4, 4, 1, 1000, 96),      # a single query row (decode-like)
+    ("fp16", 2, 2, 1, 255, 256, 64),
+    ("bf16", 1, 2, 2, 128, 1, 64),       # a single key: O = V_0, dQ = dK = 0
+    ("fp32", 1, 2, 2, 50, 200, 64),
+    ("fp32", 2, 4, 2, 130, 33, 128),
+]
+
+
+@pytest.mark.parametrize("case", CROSS_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_cross_attention_elementwise(case):
+    dtype, B, H, HKV, Tq, Tk, D = case
+    inp = make_cross_inputs(dtype, B, H, HKV, Tq, Tk, D, seed=4000 + Tq + Tk)
+    w = Workload(105, "cross", dtype, B, H, HKV, Tq, D, 0, False, True, "normal")
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, scale=w.scale, causal=False)
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, lse, do, scale=w.scale, causal=False)
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, f"device error word {word:#x}"
+    assert dk.shape == k.shape and lse.shape == (B, H, Tq)
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    O, LSE = oracle.fwd(Q, K, V, w.scale, False, 0)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, False, 0)
+    got = {n: t.float().cpu().numpy().astype(np.float64) for n, t in dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv).items()}
+    check_fwd(w, got["o"], O, got["lse"], LSE)
+    check_grad(w, "dQ", got["dq"], dQ)
+    check_grad(w, "dK", got["dk"], dK)
+    check_grad(w, "dV", got["dv"], dV)
+
+
+def test_cross_attention_rejects_masks():
+    inp = make_cross_inputs("bf16", 1, 2, 2, 64, 96, 64, seed=1)
+    dev = torch.device("cuda", 0)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    for kw in (dict(causal=True), dict(causal=False, window=16)):
+        with pytest.raises(fa.FaError) as e:
+            fa.attention_fwd(q, k, v, **kw)
+        assert e.value.status == fa.FA_ERR_UNSUPPORTED
 
 
 def test_backward_is_bitwise_reproducible():
