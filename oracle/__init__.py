@@ -70,10 +70,13 @@ def _bind(lib):
     lib.oracle_triu_offsets.argtypes = [ctypes.c_int, ctypes.c_int, _I, ctypes.c_int]
     lib.oracle_qk_norm_rope_fwd.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 4
     lib.oracle_qk_norm_rope_bwd.argtypes = [_D, _D, _D, _D, _D, _D] + [ctypes.c_int] * 4
+    lib.oracle_qk_norm_rope_fwd_opt.argtypes = [_D, _D, _D, _D, _D] + [ctypes.c_int] * 6
+    lib.oracle_qk_norm_rope_bwd_opt.argtypes = [_D, _D, _D, _D, _D, _D] + [ctypes.c_int] * 6
     for name in ("oracle_attn_probs", "oracle_attn_fwd", "oracle_attn_bwd",
                  "oracle_attn_fwd_rows", "oracle_attn_dq_rows",
                  "oracle_attn_dkdv_rows", "oracle_triu_offsets",
-                 "oracle_qk_norm_rope_fwd", "oracle_qk_norm_rope_bwd"):
+                 "oracle_qk_norm_rope_fwd", "oracle_qk_norm_rope_bwd",
+                 "oracle_qk_norm_rope_fwd_opt", "oracle_qk_norm_rope_bwd_opt"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -268,4 +271,35 @@ def qk_norm_rope_bwd(dq, dk, qk, f1, f2):
     dqk = np.empty_like(qk)
     _check(_load().oracle_qk_norm_rope_bwd(_p(dq), _p(dk), _p(qk), _p(f1), _p(f2), _p(dqk), tokens, hq, hk, D),
            "oracle_qk_norm_rope_bwd")
+    return dqk
+
+
+def qk_norm_rope_fwd_opt(qk, f1, f2, heads: int, rot: int, paired: bool, key_offset: bool):
+    """(q, k) of the prologue with equally many query and key heads and the
+    paired-heads or key-offset option: each [tokens, heads, D], or
+    [2*tokens, heads/2, D] when paired (factor rows then 2*D wide)."""
+    qk, f1, f2 = _f64(qk), _f64(f1), _f64(f2)
+    tokens, heads2, D = qk.shape
+    if heads2 != 2 * heads:
+        raise ValueError("qk must hold 2*heads heads")
+    shape = (2 * tokens, heads // 2, D) if paired else (tokens, heads, D)
+    q = np.empty(shape, np.float64)
+    k = np.empty(shape, np.float64)
+    _check(_load().oracle_qk_norm_rope_fwd_opt(_p(qk), _p(f1), _p(f2), _p(q), _p(k), tokens, int(heads), D,
+                                               int(rot), int(bool(paired)), int(bool(key_offset))),
+           "oracle_qk_norm_rope_fwd_opt")
+    return q, k
+
+
+def qk_norm_rope_bwd_opt(dq, dk, qk, f1, f2, heads: int, rot: int, paired: bool, key_offset: bool):
+    """Gradient of qk for qk_norm_rope_fwd_opt given the gradients of q and k."""
+    dq, dk, qk, f1, f2 = _f64(dq), _f64(dk), _f64(qk), _f64(f1), _f64(f2)
+    tokens, heads2, D = qk.shape
+    if heads2 != 2 * heads:
+        raise ValueError("qk must hold 2*heads heads")
+    dqk = np.empty_like(qk)
+    _check(_load().oracle_qk_norm_rope_bwd_opt(_p(dq), _p(dk), _p(qk), _p(f1), _p(f2), _p(dqk), tokens,
+                                               int(heads), D, int(rot), int(bool(paired)),
+                                               int(bool(key_offset))),
+           "oracle_qk_norm_rope_bwd_opt")
     return dqk

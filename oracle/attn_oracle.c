@@ -560,3 +560,110 @@ int oracle_qk_norm_rope_bwd(const double* dq, const double* dk, const double* qk
   }
   return 0;
 }
+
+/* --------------------------------------------------------------------------
+ * Prologue options: paired heads and key offset (the same page's
+ * `_qk_norm_rope_forward_kernel`, PAIRED and KEY_OFFSET branches, and the
+ * norm/rotary part of `_qkv_norm_rope_pack_fp8_backward_kernel`).  Here the
+ * projection has equally many query and key heads: qk[t][c][d] with
+ * c < heads a query head and heads <= c < 2*heads a key head, logical head
+ * h = c mod heads.  The two options are not combined (the page asserts so).
+ *
+ * Paired heads (heads even): factor rows are 2*D wide, head h rotates with
+ * half (h mod 2) of its token's row, and the output of (t, h) goes to output
+ * token 2t + h div (heads/2), output head h mod (heads/2); q and k are then
+ * [2*tokens][heads/2][D].
+ *
+ * Key offset (rot even, 0 <= rot <= D): for a key head of token t > 0 the
+ * stationary dims d >= rot of the output are the previous token's
+ * normalised values of the same head, unrotated:  y_d = rstd' x'_d  with x'
+ * = qk[t-1][c].  Token 0 and all query heads are unchanged.
+ *
+ * Backward: the exact gradient of this forward.  With key offset, n_e of a
+ * key row at a stationary dim e >= rot reaches only the next token's output
+ * (and, for token 0, its own rotated output), so
+ *   gn_e = [t == 0] (f1_e g_e + f2_{e^1} g_{e^1}) + [t + 1 < tokens] g'_e
+ * with g' the gradient of token t+1's key output; the page's kernel writes
+ * g_e instead of the bracketed rotation term, which is the same value when
+ * the stationary dims' factors are the identity (f1 = 1, f2 = 0).
+ * ------------------------------------------------------------------------ */
+
+static size_t qk_out_index(int t, int h, int heads, int D, int paired) {
+  if (paired) {
+    const int half = heads / 2;
+    return ((size_t)(2 * t + h / half) * half + (h % half)) * D;
+  }
+  return ((size_t)t * heads + h) * D;
+}
+
+int oracle_qk_norm_rope_fwd_opt(const double* qk, const double* f1, const double* f2, double* q, double* k,
+                                int tokens, int heads, int D, int rot, int paired, int key_offset) {
+  if (tokens < 1 || heads < 1 || D < 2 || D % 2 || (paired && key_offset)) return 1;
+  if (paired && heads % 2) return 1;
+  if (key_offset && (rot < 0 || rot > D || rot % 2)) return 1;
+  const int F = paired ? 2 * D : D;
+#pragma omp parallel for schedule(static)
+  for (long t = 0; t < tokens; ++t) {
+    for (int c = 0; c < 2 * heads; ++c) {
+      const int h = c % heads;
+      const int is_key = c >= heads;
+      const double* x = qk + ((size_t)t * 2 * heads + c) * D;
+      const double rstd = qk_rstd(x, D);
+      const double* a = f1 + (size_t)t * F + (paired ? (h % 2) * D : 0);
+      const double* b = f2 + (size_t)t * F + (paired ? (h % 2) * D : 0);
+      double* y = (is_key ? k : q) + qk_out_index((int)t, h, heads, D, paired);
+      for (int d = 0; d < D; ++d) y[d] = a[d] * (x[d] * rstd) + b[d] * (x[d ^ 1] * rstd);
+      if (key_offset && is_key && t > 0) {
+        const double* xp = qk + ((size_t)(t - 1) * 2 * heads + c) * D;
+        const double rp = qk_rstd(xp, D);
+        for (int d = rot; d < D; ++d) y[d] = xp[d] * rp;
+      }
+    }
+  }
+  return 0;
+}
+
+int oracle_qk_norm_rope_bwd_opt(const double* dq, const double* dk, const double* qk, const double* f1,
+                                const double* f2, double* dqk, int tokens, int heads, int D, int rot, int paired,
+                                int key_offset) {
+  if (tokens < 1 || heads < 1 || D < 2 || D % 2 || (paired && key_offset)) return 1;
+  if (paired && heads % 2) return 1;
+  if (key_offset && (rot < 0 || rot > D || rot % 2)) return 1;
+  const int F = paired ? 2 * D : D;
+  int status = 0;
+#pragma omp parallel
+  {
+    double* gn = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!gn) {
+#pragma omp atomic write
+      status = 2;
+    } else {
+#pragma omp for schedule(static)
+      for (long t = 0; t < tokens; ++t) {
+        for (int c = 0; c < 2 * heads; ++c) {
+          const int h = c % heads;
+          const int is_key = c >= heads;
+          const double* x = qk + ((size_t)t * 2 * heads + c) * D;
+          const double* g = (is_key ? dk : dq) + qk_out_index((int)t, h, heads, D, paired);
+          const double* a = f1 + (size_t)t * F + (paired ? (h % 2) * D : 0);
+          const double* b = f2 + (size_t)t * F + (paired ? (h % 2) * D : 0);
+          const int shifted = key_offset && is_key;
+          for (int e = 0; e < D; ++e) {
+            const int own = !shifted || t == 0 || e < rot;  /* does this row's own output use n_e? */
+            gn[e] = own ? a[e] * g[e] + b[e ^ 1] * g[e ^ 1] : 0.0;
+            if (shifted && e >= rot && t + 1 < tokens)
+              gn[e] += dk[qk_out_index((int)t + 1, h, heads, D, paired) + e];
+          }
+          const double rstd = qk_rstd(x, D);
+          double corr = 0.0;
+          for (int e = 0; e < D; ++e) corr += gn[e] * (x[e] * rstd);
+          corr /= D;
+          double* dx = dqk + ((size_t)t * 2 * heads + c) * D;
+          for (int e = 0; e < D; ++e) dx[e] = rstd * (gn[e] - (x[e] * rstd) * corr);
+        }
+      }
+      free(gn);
+    }
+  }
+  return status;
+}

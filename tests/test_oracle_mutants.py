@@ -185,8 +185,49 @@ def _pin_cross():
     return True
 
 
+def _pin_prologue_options():
+    """Paired heads relocate base outputs; key offset shifts the stationary
+    key dims by one token; both backward modes match finite differences."""
+    rng = np.random.default_rng(10)
+    tokens, heads, D, rot = 3, 4, 4, 2
+    qk = rng.standard_normal((tokens, 2 * heads, D))
+    f1, f2 = rng.standard_normal((tokens, 2 * D)), rng.standard_normal((tokens, 2 * D))
+    q, k = oracle.qk_norm_rope_fwd_opt(qk, f1, f2, heads, D, True, False)
+    for half in (0, 1):
+        bq, bk = oracle.qk_norm_rope_fwd(qk, f1[:, half * D:(half + 1) * D], f2[:, half * D:(half + 1) * D], heads)
+        for t in range(tokens):
+            for h in range(half, heads, 2):
+                pos = (2 * t + h // (heads // 2), h % (heads // 2))
+                if not (np.allclose(q[pos], bq[t, h], atol=1e-13) and np.allclose(k[pos], bk[t, h], atol=1e-13)):
+                    return False
+    g1, g2 = f1[:, :D], f2[:, :D]
+    q, k = oracle.qk_norm_rope_fwd_opt(qk, g1, g2, heads, rot, False, True)
+    bq, bk = oracle.qk_norm_rope_fwd(qk, g1, g2, heads)
+    _, nk = oracle.qk_norm_rope_fwd(qk, np.ones((tokens, D)), np.zeros((tokens, D)), heads)
+    if not (np.allclose(q, bq, atol=1e-13) and np.allclose(k[0], bk[0], atol=1e-13)
+            and np.allclose(k[1:, :, :rot], bk[1:, :, :rot], atol=1e-13)
+            and np.allclose(k[1:, :, rot:], nk[:-1, :, rot:], atol=1e-13)):
+        return False
+    for paired, key_offset, a, b in ((True, False, f1, f2), (False, True, g1, g2)):
+        shape = (2 * tokens, heads // 2, D) if paired else (tokens, heads, D)
+        gq, gk = rng.standard_normal(shape), rng.standard_normal(shape)
+        dqk = oracle.qk_norm_rope_bwd_opt(gq, gk, qk, a, b, heads, rot, paired, key_offset)
+        h = 1e-6
+        for idx in np.ndindex(qk.shape):
+            xp, xm = qk.copy(), qk.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            lp = sum(float(np.sum(o * g)) for o, g in zip(oracle.qk_norm_rope_fwd_opt(xp, a, b, heads, rot, paired,
+                                                                                       key_offset), (gq, gk)))
+            lm = sum(float(np.sum(o * g)) for o, g in zip(oracle.qk_norm_rope_fwd_opt(xm, a, b, heads, rot, paired,
+                                                                                       key_offset), (gq, gk)))
+            if abs((lp - lm) / (2 * h) - dqk[idx]) > 1e-6 * max(1.0, abs(dqk[idx])):
+                return False
+    return True
+
+
 PINS = {"sdpa+lse": _pin_sdpa, "rows": _pin_rows_match_full, "triu": _pin_triu, "fd": _pin_finite_differences,
-        "prologue": _pin_prologue, "cross": _pin_cross}
+        "prologue": _pin_prologue, "cross": _pin_cross, "prologue options": _pin_prologue_options}
 
 
 def _failing_pins():
@@ -231,6 +272,17 @@ MUTANTS = [
      "double* row = P + (size_t)i * T;", 0),
     ("dK/dV rows: Delta over the query length", "for (long j = 0; j < Tk; ++j) delta += P[j] * dP[j];",
      "for (long j = 0; j < T; ++j) delta += P[j] * dP[j];", 1),
+    ("paired factor half ignored", "const double* a = f1 + (size_t)t * F + (paired ? (h % 2) * D : 0);\n"
+     "      const double* b = f2 + (size_t)t * F + (paired ? (h % 2) * D : 0);\n      double* y",
+     "const double* a = f1 + (size_t)t * F;\n      const double* b = f2 + (size_t)t * F;\n      double* y", 0),
+    ("paired output token by head parity", "return ((size_t)(2 * t + h / half) * half + (h % half)) * D;",
+     "return ((size_t)(2 * t + h % 2) * half + (h % half)) * D;", 0),
+    ("key offset reads its own token", "const double* xp = qk + ((size_t)(t - 1) * 2 * heads + c) * D;",
+     "const double* xp = qk + ((size_t)t * 2 * heads + c) * D;", 0),
+    ("stationary gradient misses the next token", "gn[e] += dk[qk_out_index((int)t + 1, h, heads, D, paired) + e];",
+     "gn[e] += 0.0;", 0),
+    ("rotation gradient kept on shifted dims", "const int own = !shifted || t == 0 || e < rot;",
+     "const int own = 1;", 0),
     ("row LSE missing in dq rows", "softmax_row(P, Tk);\n        dp_row(&s, V, dO, b, h, i, dP);\n        double delta",
      "dp_row(&s, V, dO, b, h, i, dP);\n        double delta", 0),
 ]

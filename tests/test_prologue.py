@@ -97,6 +97,83 @@ def test_backward_matches_finite_differences():
         assert abs(fd - dqk[idx]) <= 1e-6 * max(1.0, abs(dqk[idx])), (idx, fd, dqk[idx])
 
 
+# ------------------------------------------ options: paired heads, key offset
+#
+# Pinned against the base mode (itself pinned above) and finite differences:
+#   * paired: output (t, h) is the base output of (t, h) computed with factor
+#     half h mod 2, stored at token 2t + h div (heads/2), head h mod (heads/2);
+#   * key offset: queries and token 0 equal the base output; a later key
+#     row's rotating dims equal the base output and its stationary dims the
+#     previous token's normalised values (the base output under identity
+#     factors);
+#   * both backward modes equal central differences of the forward.
+
+
+def _opt_inputs(tokens, heads, D, seed, paired):
+    rng = np.random.default_rng(seed)
+    qk = rng.standard_normal((tokens, 2 * heads, D))
+    F = 2 * D if paired else D
+    return qk, rng.standard_normal((tokens, F)), rng.standard_normal((tokens, F))
+
+
+def test_paired_heads_relocate_base_outputs():
+    tokens, heads, D = 3, 4, 6
+    qk, f1, f2 = _opt_inputs(tokens, heads, D, 21, True)
+    q, k = oracle.qk_norm_rope_fwd_opt(qk, f1, f2, heads, D, True, False)
+    assert q.shape == (2 * tokens, heads // 2, D)
+    for half in (0, 1):
+        bq, bk = oracle.qk_norm_rope_fwd(qk, f1[:, half * D:(half + 1) * D], f2[:, half * D:(half + 1) * D], heads)
+        for t in range(tokens):
+            for h in range(half, heads, 2):
+                pos = (2 * t + h // (heads // 2), h % (heads // 2))
+                np.testing.assert_array_equal(q[pos], bq[t, h])
+                np.testing.assert_array_equal(k[pos], bk[t, h])
+
+
+@pytest.mark.parametrize("rot", [0, 2, 4, 8])
+def test_key_offset_shifts_stationary_key_dims(rot):
+    tokens, heads, D = 4, 2, 8
+    qk, f1, f2 = _opt_inputs(tokens, heads, D, 22 + rot, False)
+    q, k = oracle.qk_norm_rope_fwd_opt(qk, f1, f2, heads, rot, False, True)
+    bq, bk = oracle.qk_norm_rope_fwd(qk, f1, f2, heads)
+    _, nk = oracle.qk_norm_rope_fwd(qk, np.ones((tokens, D)), np.zeros((tokens, D)), heads)
+    np.testing.assert_array_equal(q, bq)
+    np.testing.assert_array_equal(k[0], bk[0])
+    np.testing.assert_array_equal(k[1:, :, :rot], bk[1:, :, :rot])
+    np.testing.assert_allclose(k[1:, :, rot:], nk[:-1, :, rot:], rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("paired,key_offset,rot", [(False, False, 4), (True, False, 4), (False, True, 2),
+                                                    (False, True, 0), (False, True, 4)])
+def test_option_backward_matches_finite_differences(paired, key_offset, rot):
+    tokens, heads, D = 3, 2, 4
+    qk, f1, f2 = _opt_inputs(tokens, heads, D, 23 + rot, paired)
+    rng = np.random.default_rng(24)
+    shape = (2 * tokens, heads // 2, D) if paired else (tokens, heads, D)
+    gq, gk = rng.standard_normal(shape), rng.standard_normal(shape)
+    dqk = oracle.qk_norm_rope_bwd_opt(gq, gk, qk, f1, f2, heads, rot, paired, key_offset)
+
+    def loss(x):
+        q, k = oracle.qk_norm_rope_fwd_opt(x, f1, f2, heads, rot, paired, key_offset)
+        return float(np.sum(q * gq) + np.sum(k * gk))
+
+    h = 1e-6
+    for idx in np.ndindex(qk.shape):
+        xp, xm = qk.copy(), qk.copy()
+        xp[idx] += h
+        xm[idx] -= h
+        fd = (loss(xp) - loss(xm)) / (2 * h)
+        assert abs(fd - dqk[idx]) <= 1e-6 * max(1.0, abs(dqk[idx])), (idx, fd, dqk[idx])
+
+
+def test_options_reject_invalid_combinations():
+    qk, f1, f2 = _opt_inputs(2, 2, 4, 25, False)
+    with pytest.raises(RuntimeError):
+        oracle.qk_norm_rope_fwd_opt(qk, f1, f2, 2, 2, True, True)  # both options
+    with pytest.raises(RuntimeError):
+        oracle.qk_norm_rope_fwd_opt(qk, f1, f2, 2, 3, False, True)  # odd rotary dim
+
+
 # ------------------------------------------------------------------ GPU
 
 def _dev():
