@@ -35,14 +35,18 @@ from ._binding import (  # noqa: F401
     fa_plan_kv_range,
     fa_plan_q_range,
     fa_qk_norm_rope_bwd,
+    fa_qk_norm_rope_bwd_opt,
     fa_qk_norm_rope_fwd,
+    fa_qk_norm_rope_fwd_opt,
     fa_status_string,
     fa_tile_m,
     fa_tile_n,
     fa_workspace_size,
     load,
     qk_norm_rope_bwd,
+    qk_norm_rope_bwd_opt,
     qk_norm_rope_fwd,
+    qk_norm_rope_fwd_opt,
 )
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -99,6 +99,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_qk_norm_rope_fwd.restype = _i
         lib.fa_qk_norm_rope_bwd.argtypes = [_vp] * 6 + [_i] * 5 + [_vp]
         lib.fa_qk_norm_rope_bwd.restype = _i
+        lib.fa_qk_norm_rope_fwd_opt.argtypes = [_vp] * 5 + [_i] * 7 + [_vp]
+        lib.fa_qk_norm_rope_fwd_opt.restype = _i
+        lib.fa_qk_norm_rope_bwd_opt.argtypes = [_vp] * 6 + [_i] * 7 + [_vp]
+        lib.fa_qk_norm_rope_bwd_opt.restype = _i
         _lib = lib
         return lib
 
@@ -204,6 +208,18 @@ def fa_qk_norm_rope_fwd(qk, f1, f2, q, k, tokens, hq, hk, head_dim, dtype, strea
 
 def fa_qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk, tokens, hq, hk, head_dim, dtype, stream) -> int:
     return load().fa_qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk, tokens, hq, hk, head_dim, dtype, stream)
+
+
+def fa_qk_norm_rope_fwd_opt(qk, f1, f2, q, k, tokens, heads, head_dim, rotary_dim, paired, key_offset, dtype,
+                            stream) -> int:
+    return load().fa_qk_norm_rope_fwd_opt(qk, f1, f2, q, k, tokens, heads, head_dim, rotary_dim, paired,
+                                          key_offset, dtype, stream)
+
+
+def fa_qk_norm_rope_bwd_opt(dq, dk, qk, f1, f2, dqk, tokens, heads, head_dim, rotary_dim, paired, key_offset,
+                            dtype, stream) -> int:
+    return load().fa_qk_norm_rope_bwd_opt(dq, dk, qk, f1, f2, dqk, tokens, heads, head_dim, rotary_dim, paired,
+                                          key_offset, dtype, stream)
 
 
 # ------------------------------------------------------------ torch layer
@@ -388,4 +404,49 @@ def qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk=None, stream=None):
                              dqk.data_ptr(), tokens, hq, hk, D, dt, _stream(dev, stream))
     if st != FA_OK:
         raise FaError(st, "fa_qk_norm_rope_bwd")
+    return dqk
+
+
+def qk_norm_rope_fwd_opt(qk, f1, f2, heads, rotary_dim=0, paired=False, key_offset=False, stream=None):
+    """Prologue with the paired-heads or key-offset option: qk [tokens,
+    2*heads, D] -> (q, k), each [tokens, heads, D] or, paired,
+    [2*tokens, heads/2, D] (f1, f2 then [tokens, 2*D])."""
+    torch = _torch()
+    tokens, heads2, D = qk.shape
+    dev = qk.device
+    dt = _dtype_code(qk)
+    _check_tensor("qk", qk, (tokens, 2 * int(heads), D), qk.dtype, dev)
+    F = 2 * D if paired else D
+    for name, t in (("f1", f1), ("f2", f2)):
+        _check_tensor(name, t, (tokens, F), torch.float32, dev)
+    shape = (2 * tokens, int(heads) // 2, D) if paired else (tokens, int(heads), D)
+    q = torch.empty(shape, dtype=qk.dtype, device=dev)
+    k = torch.empty(shape, dtype=qk.dtype, device=dev)
+    st = fa_qk_norm_rope_fwd_opt(qk.data_ptr(), f1.data_ptr(), f2.data_ptr(), q.data_ptr(), k.data_ptr(), tokens,
+                                 int(heads), D, int(rotary_dim), int(bool(paired)), int(bool(key_offset)), dt,
+                                 _stream(dev, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_qk_norm_rope_fwd_opt")
+    return q, k
+
+
+def qk_norm_rope_bwd_opt(dq, dk, qk, f1, f2, heads, rotary_dim=0, paired=False, key_offset=False, stream=None):
+    """Gradient of qk for qk_norm_rope_fwd_opt given the gradients of q and k."""
+    torch = _torch()
+    tokens, heads2, D = qk.shape
+    dev = qk.device
+    dt = _dtype_code(qk)
+    _check_tensor("qk", qk, (tokens, 2 * int(heads), D), qk.dtype, dev)
+    shape = (2 * tokens, int(heads) // 2, D) if paired else (tokens, int(heads), D)
+    _check_tensor("dq", dq, shape, qk.dtype, dev)
+    _check_tensor("dk", dk, shape, qk.dtype, dev)
+    F = 2 * D if paired else D
+    for name, t in (("f1", f1), ("f2", f2)):
+        _check_tensor(name, t, (tokens, F), torch.float32, dev)
+    dqk = torch.empty_like(qk)
+    st = fa_qk_norm_rope_bwd_opt(dq.data_ptr(), dk.data_ptr(), qk.data_ptr(), f1.data_ptr(), f2.data_ptr(),
+                                 dqk.data_ptr(), tokens, int(heads), D, int(rotary_dim), int(bool(paired)),
+                                 int(bool(key_offset)), dt, _stream(dev, stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_qk_norm_rope_bwd_opt")
     return dqk

@@ -415,6 +415,49 @@ int fa_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const fl
                                                static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+int qk_opt_check(int tokens, int heads, int head_dim, int rotary_dim, int paired, int key_offset, int dtype) {
+  if (tokens < 1 || heads < 1) return FA_ERR_INVALID_ARG;
+  if (paired && key_offset) return FA_ERR_INVALID_ARG;  // the options are exclusive
+  if (paired && heads % 2) return FA_ERR_INVALID_ARG;
+  if (key_offset && (rotary_dim < 0 || rotary_dim > head_dim || rotary_dim % 2)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(tokens) * 2 * heads * head_dim >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+}  // namespace
+
+int fa_qk_norm_rope_fwd_opt(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens,
+                            int heads, int head_dim, int rotary_dim, int paired, int key_offset, int dtype,
+                            void* stream) {
+  int st = qk_opt_check(tokens, heads, head_dim, rotary_dim, paired, key_offset, dtype);
+  if (st != FA_OK) return st;
+  const void* ptrs[5] = {qk, f1, f2, q, k};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  int dev;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  return status_of(fa::launch_qk_norm_rope_fwd_opt(qk, f1, f2, q, k, tokens, heads, head_dim, rotary_dim,
+                                                   paired != 0, key_offset != 0, dtype == FA_DTYPE_FP16,
+                                                   g_dev[dev].sms, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_qk_norm_rope_bwd_opt(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2,
+                            void* dqk, int tokens, int heads, int head_dim, int rotary_dim, int paired, int key_offset,
+                            int dtype, void* stream) {
+  int st = qk_opt_check(tokens, heads, head_dim, rotary_dim, paired, key_offset, dtype);
+  if (st != FA_OK) return st;
+  const void* ptrs[6] = {dq, dk, qk, f1, f2, dqk};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return FA_ERR_INVALID_ARG;
+  int dev;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  return status_of(fa::launch_qk_norm_rope_bwd_opt(dq, dk, qk, f1, f2, dqk, tokens, heads, head_dim, rotary_dim,
+                                                   paired != 0, key_offset != 0, dtype == FA_DTYPE_FP16,
+                                                   g_dev[dev].sms, static_cast<cudaStream_t>(stream)));
+}
+
 int fa_tile_m(void) { return fa::kBM; }
 int fa_tile_n(void) { return fa::kBN; }
 

@@ -101,6 +101,14 @@ struct TensorMaps {
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
 // Pre-attention prologue (RMS-norm + rotary of the packed QK projection).
+// Prologue with equally many query and key heads and the paired-heads or
+// key-offset option (never both; neither = the plain prologue).
+cudaError_t launch_qk_norm_rope_fwd_opt(const void* qk, const float* f1, const float* f2, void* q, void* k,
+                                        int tokens, int heads, int D, int rot, bool paired, bool key_offset, bool f16,
+                                        int sms, cudaStream_t stream);
+cudaError_t launch_qk_norm_rope_bwd_opt(const void* dq, const void* dk, const void* qk, const float* f1,
+                                        const float* f2, void* dqk, int tokens, int heads, int D, int rot,
+                                        bool paired, bool key_offset, bool f16, int sms, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens,
                                     int hq, int hk, int D, bool f16, int sms, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2,

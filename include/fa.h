@@ -257,6 +257,37 @@ int fa_qk_norm_rope_fwd(const void* qk, const float* f1, const float* f2, void* 
 int fa_qk_norm_rope_bwd(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2, void* dqk,
                         int tokens, int hq, int hk, int head_dim, int dtype, void* stream);
 
+/*
+ * The same prologue with its two options (the modded-nanogpt qkv_rope.py
+ * page, `_qk_norm_rope_forward_kernel`, PAIRED and KEY_OFFSET branches, and
+ * the norm/rotary part of `_qkv_norm_rope_pack_fp8_backward_kernel`), for a
+ * projection with equally many query and key heads:
+ *   qk [tokens][2*heads][head_dim]: heads 0..heads-1 are queries, the rest
+ *   keys; logical head h = c mod heads.
+ *   paired (heads even): f1, f2 [tokens][2*head_dim]; head h rotates with
+ *     factor half h mod 2 and is written to token 2t + h / (heads/2), head
+ *     h mod (heads/2) of q, k [2*tokens][heads/2][head_dim].
+ *   key_offset: f1, f2 [tokens][head_dim]; q, k [tokens][heads][head_dim];
+ *     a key row of token t > 0 takes dims d >= rotary_dim (even, 0..head_dim)
+ *     from token t-1's normalised row of the same head, unrotated
+ *     (y_d = x'_d / sqrt(mean(x'^2) + 2^-23)).  Token 0 and the queries are
+ *     the plain prologue.
+ *   Neither option: the plain prologue with hq = hk = heads (rotary_dim is
+ *   ignored unless key_offset is set).
+ * The backward is the exact gradient of this forward (for key offset, a key
+ * row's stationary dims get the gradient of token t+1's key output, plus the
+ * rotation term at t = 0); dq, dk have the forward's output shapes and dqk
+ * the shape of qk.
+ * Errors: both options, an odd head count with paired, or a bad rotary_dim
+ * with key_offset: FA_ERR_INVALID_ARG; otherwise as fa_qk_norm_rope_fwd.
+ */
+int fa_qk_norm_rope_fwd_opt(const void* qk, const float* f1, const float* f2, void* q, void* k, int tokens,
+                            int heads, int head_dim, int rotary_dim, int paired, int key_offset, int dtype,
+                            void* stream);
+int fa_qk_norm_rope_bwd_opt(const void* dq, const void* dk, const void* qk, const float* f1, const float* f2,
+                            void* dqk, int tokens, int heads, int head_dim, int rotary_dim, int paired, int key_offset,
+                            int dtype, void* stream);
+
 /* Tile sizes the bf16 kernels use (query rows, key rows per block). */
 int fa_tile_m(void);
 int fa_tile_n(void);

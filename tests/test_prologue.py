@@ -218,6 +218,47 @@ def test_gpu_matches_oracle(case):
     assert np.linalg.norm(got - dX) / np.linalg.norm(dX) <= 2e-2
 
 
+OPT_CASES = [  # tokens, heads, D, rot, paired, key_offset, dtype
+    (37, 4, 64, 0, True, False, torch.bfloat16),
+    (19, 2, 128, 0, True, False, torch.float16),
+    (33, 2, 64, 32, False, True, torch.bfloat16),
+    (9, 3, 128, 96, False, True, torch.float16),
+    (5, 2, 64, 0, False, True, torch.bfloat16),     # every dim stationary
+    (12, 2, 128, 128, False, True, torch.bfloat16),  # no stationary dim: the plain prologue
+    (21, 3, 64, 0, False, False, torch.bfloat16),    # neither option
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", OPT_CASES, ids=lambda c: "-".join(str(x) for x in c[:6]) + "-" + str(c[6])[6:])
+def test_gpu_options_match_oracle(case):
+    import flash_attention_attn_gb300 as fa
+    tokens, heads, D, rot, paired, key_offset, dt = case
+    dev = _dev()
+    qk, f1, f2 = _opt_inputs(tokens, heads, D, 300 + tokens, paired)
+    shape = (2 * tokens, heads // 2, D) if paired else (tokens, heads, D)
+    rng = np.random.default_rng(400 + tokens)
+    gq, gk = rng.standard_normal(shape), rng.standard_normal(shape)
+    qk_t = torch.tensor(qk, dtype=torch.float32).to(dt)
+    gq_t = torch.tensor(gq, dtype=torch.float32).to(dt)
+    gk_t = torch.tensor(gk, dtype=torch.float32).to(dt)
+    f1_t, f2_t = (torch.tensor(f, dtype=torch.float32) for f in (f1, f2))
+    q, k = fa.qk_norm_rope_fwd_opt(qk_t.to(dev), f1_t.to(dev), f2_t.to(dev), heads, rot, paired, key_offset)
+    dqk = fa.qk_norm_rope_bwd_opt(gq_t.to(dev), gk_t.to(dev), qk_t.to(dev), f1_t.to(dev), f2_t.to(dev), heads, rot,
+                                  paired, key_offset)
+    torch.cuda.synchronize()
+    x64 = qk_t.double().numpy()
+    Q, K = oracle.qk_norm_rope_fwd_opt(x64, f1, f2, heads, rot, paired, key_offset)
+    dX = oracle.qk_norm_rope_bwd_opt(gq_t.double().numpy(), gk_t.double().numpy(), x64, f1, f2, heads, rot, paired,
+                                     key_offset)
+    half_ulp = 2.0 ** -8 if dt == torch.bfloat16 else 2.0 ** -11
+    for got, ref in ((q, Q), (k, K)):
+        err = np.abs(got.double().cpu().numpy() - ref)
+        assert np.all(err <= half_ulp * np.abs(ref) + 1e-4), float(np.max(err - half_ulp * np.abs(ref)))
+    got = dqk.double().cpu().numpy()
+    assert np.linalg.norm(got - dX) / np.linalg.norm(dX) <= 2e-2
+
+
 def test_abi_argument_checks():
     from flash_attention_attn_gb300 import _binding as fb
     from flash_attention_attn_gb300.build import build
@@ -240,3 +281,29 @@ def test_abi_argument_checks():
     assert fb.fa_qk_norm_rope_bwd(*p, 4, 2, 2, 100, fb.FA_DTYPE_BF16, None) == fb.FA_ERR_UNSUPPORTED
     if not torch.cuda.is_available():
         assert fwd() in (fb.FA_ERR_CUDA, fb.FA_ERR_UNSUPPORTED)  # no device: an error, never a fallback
+
+
+def test_abi_option_argument_checks():
+    from flash_attention_attn_gb300 import _binding as fb
+    from flash_attention_attn_gb300.build import build
+    build()
+    fake = 0x10000
+
+    def fwd(tokens=4, heads=2, D=64, rot=32, paired=0, key_offset=1, dtype=fb.FA_DTYPE_BF16, ptrs=None):
+        p = ptrs or [fake] * 5
+        return fb.fa_qk_norm_rope_fwd_opt(*p, tokens, heads, D, rot, paired, key_offset, dtype, None)
+
+    assert fwd(tokens=0) == fb.FA_ERR_INVALID_ARG
+    assert fwd(paired=1, key_offset=1) == fb.FA_ERR_INVALID_ARG  # the options are exclusive
+    assert fwd(paired=1, key_offset=0, heads=3) == fb.FA_ERR_INVALID_ARG
+    assert fwd(rot=33) == fb.FA_ERR_INVALID_ARG
+    assert fwd(rot=66) == fb.FA_ERR_INVALID_ARG
+    assert fwd(rot=-2) == fb.FA_ERR_INVALID_ARG
+    assert fwd(D=96) == fb.FA_ERR_UNSUPPORTED
+    assert fwd(dtype=fb.FA_DTYPE_FP32) == fb.FA_ERR_UNSUPPORTED
+    assert fwd(ptrs=[fake, fake, fake + 4, fake, fake]) == fb.FA_ERR_INVALID_ARG
+    p = [fake] * 6
+    assert fb.fa_qk_norm_rope_bwd_opt(*p, 4, 2, 64, 0, 1, 1, fb.FA_DTYPE_BF16, None) == fb.FA_ERR_INVALID_ARG
+    assert fb.fa_qk_norm_rope_bwd_opt(*p, 4, 2, 64, 3, 0, 1, fb.FA_DTYPE_BF16, None) == fb.FA_ERR_INVALID_ARG
+    if not torch.cuda.is_available():
+        assert fwd() in (fb.FA_ERR_CUDA, fb.FA_ERR_UNSUPPORTED)
