@@ -86,6 +86,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             getattr(lib, name).argtypes = [_i] * 6 + [ctypes.POINTER(_i), ctypes.POINTER(_i)]
             getattr(lib, name).restype = _i
         lib.fa_plan_block_mask.argtypes = [_i] * 7
+        for name in ("fa_plan_row_keys", "fa_plan_key_rows"):
+            getattr(lib, name).argtypes = [_i] * 5 + [ctypes.POINTER(_i), ctypes.POINTER(_i)]
+            getattr(lib, name).restype = _i
         lib.fa_plan_block_mask.restype = _i
         lib.fa_tile_m.argtypes = []
         lib.fa_tile_m.restype = _i
@@ -171,6 +174,22 @@ def fa_plan_kv_range(T, BM, BN, causal, window, qb):
     st = load().fa_plan_kv_range(T, BM, BN, causal, window, qb, ctypes.byref(lo), ctypes.byref(hi))
     if st:
         raise FaError(st, "fa_plan_kv_range")
+    return lo.value, hi.value
+
+
+def fa_plan_row_keys(Tq, Tk, causal, window, i):
+    lo, hi = _i(0), _i(0)
+    st = load().fa_plan_row_keys(Tq, Tk, causal, window, i, ctypes.byref(lo), ctypes.byref(hi))
+    if st:
+        raise FaError(st, "fa_plan_row_keys")
+    return lo.value, hi.value
+
+
+def fa_plan_key_rows(Tq, Tk, causal, window, j):
+    lo, hi = _i(0), _i(0)
+    st = load().fa_plan_key_rows(Tq, Tk, causal, window, j, ctypes.byref(lo), ctypes.byref(hi))
+    if st:
+        raise FaError(st, "fa_plan_key_rows")
     return lo.value, hi.value
 
 

@@ -119,10 +119,13 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 }  // namespace
 
 namespace fa {
-bool fwd_two_tiles(const Shape& s) {
+int fwd_mode(const Shape& s) {
+  const bool heads_pair = (s.H / s.HKV) % 2 == 0;
   const int forced = g_fwd_tiles.load();
-  if (forced != 0) return forced == 2;
-  return ceil_div(s.T, kBM) >= 2;
+  if (forced == 1 || forced == 2) return forced;
+  if (heads_pair) return 3;
+  if (forced == 3) return ceil_div(s.T, kBM) >= 2 ? 2 : 1;
+  return ceil_div(s.T, kBM) >= 2 ? 2 : 1;
 }
 }  // namespace fa
 
@@ -379,6 +382,18 @@ int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* 
   return FA_OK;
 }
 
+int fa_plan_row_keys(int Tq, int Tk, int causal, int window, int i, int* lo, int* hi) {
+  if (Tq < 1 || Tk < 1 || window < 0 || i < 0 || !lo || !hi) return FA_ERR_INVALID_ARG;
+  fa::visible_keys(Tq, Tk, causal, window, i, *lo, *hi);
+  return FA_OK;
+}
+
+int fa_plan_key_rows(int Tq, int Tk, int causal, int window, int j, int* lo, int* hi) {
+  if (Tq < 1 || Tk < 1 || window < 0 || j < 0 || !lo || !hi) return FA_ERR_INVALID_ARG;
+  fa::visible_queries(Tq, Tk, causal, window, j, *lo, *hi);
+  return FA_OK;
+}
+
 int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb) {
   if (T < 1 || BM < 1 || BN < 1 || window < 0 || qb < 0 || kb < 0) return -FA_ERR_INVALID_ARG;
   return fa::block_needs_mask(T, T, BM, BN, causal, window, qb, kb) ? 1 : 0;
@@ -462,7 +477,7 @@ int fa_tile_m(void) { return fa::kBM; }
 int fa_tile_n(void) { return fa::kBN; }
 
 int fa_debug_fwd_tiles(int tiles) {
-  if (tiles < 0 || tiles > 2) return FA_ERR_INVALID_ARG;
+  if (tiles < 0 || tiles > 3) return FA_ERR_INVALID_ARG;
   g_fwd_tiles.store(tiles);
   return FA_OK;
 }

@@ -377,9 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         pv[4 * c4 + 3] = ex2(x3);
       }
       if (need_mask) {
+        // the visibility rule element by element (the [lo, hi] range form
+        // the other kernels use measured 3 % slower here on the long causal
+        // workload: it changed this kernel's register allocation)
         const int i0 = qb * BQ + half * 64;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.Tk, s.causal, s.window, i0 + c, j) ? 0.f : pv[c];
+        for (int c = 0; c < 64; ++c) {
+          const int i = i0 + c;
+          const bool hide = i >= s.T || j >= s.Tk || (s.causal && j > i) || (s.window > 0 && i - j >= s.window);
+          pv[c] = hide ? 0.f : pv[c];
+        }
       }
       {
         uint32_t pk[32];
@@ -602,6 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = warp >> 2;  // 64-key half of each 128-key block
     const int irow = quarter * 32 + lane;
     const int i = qb * BQ + irow;
+    int vis_lo, vis_hi;  // keys row i sees
+    visible_keys(s.T, s.Tk, s.causal, s.window, i, vis_lo, vis_hi);
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     float lse2 = 0.f, delta = 0.f;
@@ -636,9 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb)) {
-        const int j0 = kb * BK + half * 64;
+        // the keys this row sees, relative to the 64 columns
+        const int a = vis_lo - (kb * BK + half * 64), z = vis_hi - (kb * BK + half * 64);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = masked(s.T, s.Tk, s.causal, s.window, i, j0 + c) ? 0.f : pv[c];
+        for (int c = 0; c < 64; ++c) pv[c] = (c < a || c > z) ? 0.f : pv[c];
       }
       // pass 2: dS = P (dP - Delta) -> bf16 over the S columns this thread read
       if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;

@@ -221,6 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- softmax
     const int t = threadIdx.x;  // 0..127 = TMEM lane = tile row
     const int row = qb * kBM + t;
+    int vis_lo, vis_hi;  // keys this row sees
+    visible_keys(s.T, s.Tk, s.causal, s.window, row, vis_lo, vis_hi);
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = p.scale_log2;
     float m_run = -CUDART_INF_F;  // reference max, log2 domain
@@ -258,9 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         sv[96 + c] = __uint_as_float(r3[c]);
       }
       if (block_needs_mask(s.T, s.Tk, kBM, kBN, s.causal, s.window, qb, kb)) {
+        // this row's visible keys, relative to the block
+        const int a = vis_lo - kb * kBN, z = vis_hi - kb * kBN;
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (masked(s.T, s.Tk, s.causal, s.window, row, kb * kBN + c)) sv[c] = -CUDART_INF_F;
+          if (c < a || c > z) sv[c] = -CUDART_INF_F;
       }
       float mx = sv[0];
 #pragma unroll
@@ -425,15 +429,21 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nq = ceil_div(s.T, kBM);
-  const int npair = ceil_div(nq, 2);
-  const int pair = npair - 1 - static_cast<int>(blockIdx.x);  // longest causal pairs first
-  const int h = blockIdx.y;
   const int b = blockIdx.z;
-  const int g = h / (s.H / s.HKV);
+  // The two tiles: query blocks q_a, q_b of heads h_a, h_b.  Block pairs:
+  // blocks 2j and 2j + 1 of one head; head pairs: one block of heads 2j and
+  // 2j + 1, which share a KV head when H/HKV is even, so that both tiles
+  // see the same key range.  Longest causal work first.
+  const int q_a = p.pack_heads ? nq - 1 - static_cast<int>(blockIdx.x)
+                               : 2 * (ceil_div(nq, 2) - 1 - static_cast<int>(blockIdx.x));
+  const int q_b = p.pack_heads ? q_a : q_a + 1;
+  const int h_a = p.pack_heads ? 2 * static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
+  const int h_b = p.pack_heads ? h_a + 1 : h_a;
+  const int g = h_a / (s.H / s.HKV);
   // visible KV block range of each tile (B is empty past the end)
   int lo_a, hi_a, lo_b = 1, hi_b = 0;
-  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, 2 * pair, lo_a, hi_a);
-  if (2 * pair + 1 < nq) kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, 2 * pair + 1, lo_b, hi_b);
+  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, q_a, lo_a, hi_a);
+  if (q_b < nq) kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, q_b, lo_b, hi_b);
   const bool has_b = lo_b <= hi_b;
   const int lo = has_b ? imin(lo_a, lo_b) : lo_a;
   const int hi = has_b ? imax(hi_a, hi_b) : hi_a;
@@ -481,8 +491,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_arrive_expect_tx_e(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
       for (int t = 0; t < (has_b ? 2 : 1); ++t)
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64, h,
-                      (2 * pair + t) * kBM, b);
+          tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64,
+                        t ? h_b : h_a, (t ? q_b : q_a) * kBM, b);
       int issued_k = 0, issued_v = 0;
       for (int n = 0; n < nblk; ++n) {
         const int st = n % C::kKStages;
@@ -580,8 +590,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
     // -------------------------------------------------------------- softmax
     const int t = warp >> 2;   // tile
     const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
-    const int q = 2 * pair + t;
+    const int q = t ? q_b : q_a;
+    const int h = t ? h_b : h_a;
     const int row = q * kBM + r;
+    int vis_lo, vis_hi;  // keys this row sees
+    visible_keys(s.T, s.Tk, s.causal, s.window, row, vis_lo, vis_hi);
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + C::kTmS + t * 128;
     const uint32_t o_addr = tmem + lane_addr + C::kTmO + t * D;
@@ -606,9 +619,11 @@ __global__ void __launch_bounds__(kThreads2, 1)
           uint32_t ra[32];
           tmem_ld32(s_addr + c4 * 32, ra);
           tmem_ld_wait(ra);
+          // this row's visible keys, relative to the chunk
+          const int a = vis_lo - (kb * kBN + c4 * 32), z = vis_hi - (kb * kBN + c4 * 32);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (masked(s.T, s.Tk, s.causal, s.window, row, kb * kBN + c4 * 32 + c)) ra[c] = __float_as_uint(-CUDART_INF_F);
+            if (c < a || c > z) ra[c] = __float_as_uint(-CUDART_INF_F);
           tmem_st32(s_addr + c4 * 32, ra);
         }
         tmem_st_wait();
@@ -740,7 +755,8 @@ cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(ceil_div(p.s.T, kBM), 2), p.s.H, p.s.B);
+  const int nq = ceil_div(p.s.T, kBM);
+  const dim3 grid = p.pack_heads ? dim3(nq, p.s.H / 2, p.s.B) : dim3(ceil_div(nq, 2), p.s.H, p.s.B);
   fa_fwd2_bf16_kernel<D, F16><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
   return cudaGetLastError();
 }
@@ -763,8 +779,11 @@ cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t 
 }  // namespace
 
 template <bool F16>
-cudaError_t launch_fwd_t(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
-  const bool two = fwd_two_tiles(p.s);
+cudaError_t launch_fwd_t(const TensorMaps& tm, const FwdParams& p0, cudaStream_t stream) {
+  const int mode = fwd_mode(p0.s);
+  const bool two = mode >= 2;
+  FwdParams p = p0;
+  p.pack_heads = mode == 3;
   // head dims up to 64 run the 64-wide kernels, up to 128 the 128-wide ones
   if (p.s.D <= 64) return two ? launch_fwd2_d<64, F16>(tm, p, stream) : launch_fwd_d<64, F16>(tm, p, stream);
   if (p.s.D <= 128) return two ? launch_fwd2_d<128, F16>(tm, p, stream) : launch_fwd_d<128, F16>(tm, p, stream);

@@ -20,9 +20,21 @@ __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : 
 
 // Visible(i, j) = (!causal || j <= i) && (window == 0 || i - j < window),
 // with query row i < Tq and key row j < Tk (Tq = Tk for self-attention; the
-// library accepts Tq != Tk only without causal or window masking).
-__host__ __device__ __forceinline__ bool masked(int Tq, int Tk, int causal, int window, int i, int j) {
-  return i >= Tq || j >= Tk || (causal && j > i) || (window > 0 && i - j >= window);
+// library accepts Tq != Tk only without causal or window masking).  As index
+// ranges, for per-element masking inside a block: query row i sees keys
+// [lo, hi]; key j is seen by query rows [lo, hi] (empty, lo > hi, for a row
+// or key past the end).
+__host__ __device__ __forceinline__ void visible_keys(int Tq, int Tk, int causal, int window, int i, int& lo,
+                                                      int& hi) {
+  lo = window > 0 ? imax(0, i - window + 1) : 0;
+  hi = causal ? imin(i, Tk - 1) : Tk - 1;
+  if (i >= Tq) lo = hi + 1;
+}
+__host__ __device__ __forceinline__ void visible_queries(int Tq, int Tk, int causal, int window, int j, int& lo,
+                                                         int& hi) {
+  lo = causal ? j : 0;
+  hi = window > 0 ? imin(Tq - 1, j + window - 1) : Tq - 1;
+  if (j >= Tk) lo = hi + 1;
 }
 
 // KV blocks [lo, hi] that query tile qb must visit: blocks wholly above the
@@ -78,6 +90,7 @@ struct FwdParams {
   uint64_t timeout_ns;
   int inject_stall;
   int f16;            // elements are fp16 (else bf16)
+  int pack_heads;     // two-tile kernel: the tiles are one query block of two heads (else two blocks of one head)
 };
 
 struct BwdParams {
@@ -115,7 +128,10 @@ cudaError_t launch_qk_norm_rope_bwd(const void* dq, const void* dk, const void* 
                                     void* dqk, int tokens, int hq, int hk, int D, bool f16, int sms,
                                     cudaStream_t stream);
 // Whether the bf16 forward runs two query tiles per CTA for this shape.
-bool fwd_two_tiles(const Shape& s);
+// Forward kernel for a shape: 1 = one query tile per CTA, 2 = two tiles =
+// two adjacent query blocks of one head, 3 = two tiles = one query block of
+// two heads that share a KV head.
+int fwd_mode(const Shape& s);
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 

@@ -226,6 +226,15 @@ const char* fa_status_string(int status);
 int fa_plan_kv_range(int T, int BM, int BN, int causal, int window, int qb, int* lo, int* hi);
 int fa_plan_q_range(int T, int BM, int BN, int causal, int window, int kb, int* lo, int* hi);
 int fa_plan_block_mask(int T, int BM, int BN, int causal, int window, int qb, int kb);
+/*
+ * The per-element rule the kernels apply inside a block that needs a mask,
+ * as index ranges (host memory outputs): fa_plan_row_keys gives the keys
+ * [*lo, *hi] query row i sees, fa_plan_key_rows the query rows [*lo, *hi]
+ * that see key j; empty (lo > hi) past the end of the sequence.  Tq query
+ * rows, Tk key rows.  FA_ERR_INVALID_ARG for bad sizes.
+ */
+int fa_plan_row_keys(int Tq, int Tk, int causal, int window, int i, int* lo, int* hi);
+int fa_plan_key_rows(int Tq, int Tk, int causal, int window, int j, int* lo, int* hi);
 
 /*
  * Pre-attention prologue: RMS-norm of every query and key head vector of the
@@ -303,12 +312,14 @@ int fa_tile_n(void);
 int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall);
 
 /*
- * Test hook.  Query tiles per CTA of the bf16 forward: 1 (one 128-row tile),
- * 2 (two 128-row tiles sharing every K/V block the CTA streams) or 0
- * (automatic: two whenever the sequence has at least two query tiles).
- * Both produce the same O and LSE up to fp32 rounding order.  Returns
- * FA_ERR_INVALID_ARG for any other value.  Affects later calls of this
- * process only.
+ * Test hook.  Query tiles per CTA of the 16-bit forward: 1 (one 128-row
+ * tile), 2 (two 128-row tiles, adjacent query blocks of one head, sharing
+ * every K/V block the CTA streams), 3 (two tiles, the same query block of
+ * two query heads that share a KV head; needs an even H/HKV, else as 0) or 0
+ * (automatic: 3 when H/HKV is even, else 2 when the sequence has at least
+ * two query tiles, else 1).  All produce the same O and LSE up to fp32
+ * rounding order.  Returns FA_ERR_INVALID_ARG for any other value.  Affects
+ * later calls of this process only.
  */
 int fa_debug_fwd_tiles(int tiles);
 

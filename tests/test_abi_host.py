@@ -140,9 +140,9 @@ def test_no_gpu_means_error_not_fallback(lib):
 
 
 def test_forward_tiles_hook_validates(lib):
-    assert fb.fa_debug_fwd_tiles(3) == fb.FA_ERR_INVALID_ARG
+    assert fb.fa_debug_fwd_tiles(4) == fb.FA_ERR_INVALID_ARG
     assert fb.fa_debug_fwd_tiles(-1) == fb.FA_ERR_INVALID_ARG
-    for t in (1, 2, 0):
+    for t in (1, 2, 3, 0):
         assert fb.fa_debug_fwd_tiles(t) == fb.FA_OK
 
 
@@ -197,6 +197,31 @@ def test_plan_matches_brute_force(lib, T, BM, BN, causal, W):
         for qb in range(nq):
             if cols[qb * BM:(qb + 1) * BM].any():
                 assert lo <= qb <= hi
+
+
+@pytest.mark.parametrize("Tq,Tk", [(1, 1), (7, 7), (130, 130), (9, 20), (20, 9)])
+@pytest.mark.parametrize("causal,W", [(0, 0), (1, 0), (1, 3), (0, 4), (1, 1), (1, 200)])
+def test_row_key_ranges_match_brute_force(lib, Tq, Tk, causal, W):
+    """The per-element rule inside masked blocks, as ranges, against the
+    visibility rule evaluated element by element (rows and keys past the end
+    included)."""
+    i = np.arange(Tq + 3)[:, None]
+    j = np.arange(Tk + 3)[None, :]
+    vis = (i < Tq) & (j < Tk)
+    if causal:
+        vis &= j <= i
+    if W:
+        vis &= (i - j) < W
+    for r in range(Tq + 3):
+        lo, hi = fb.fa_plan_row_keys(Tq, Tk, causal, W, r)
+        want = np.flatnonzero(vis[r])
+        got = np.arange(lo, hi + 1) if lo <= hi else np.array([], int)
+        assert np.array_equal(got, want), (r, lo, hi)
+    for c in range(Tk + 3):
+        lo, hi = fb.fa_plan_key_rows(Tq, Tk, causal, W, c)
+        want = np.flatnonzero(vis[:, c])
+        got = np.arange(lo, hi + 1) if lo <= hi else np.array([], int)
+        assert np.array_equal(got, want), (c, lo, hi)
 
 
 @pytest.mark.parametrize("BM,BN", [(2, 2), (2, 3), (2, 4), (3, 5), (128, 128), (64, 128)])

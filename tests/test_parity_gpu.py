@@ -143,14 +143,20 @@ FWD_TILE_CASES = [
     ("fp16", 2, 4, 2, 300, 64, 0, True),
     ("bf16", 1, 4, 2, 513, 96, 0, True),
     ("bf16", 1, 2, 2, 300, 48, 64, True),
+    # one query tile: head pairs let GQA shapes use the two-tile kernel
+    ("bf16", 2, 8, 2, 100, 128, 0, True),
+    ("fp16", 1, 4, 2, 128, 64, 0, False),
+    ("bf16", 1, 6, 3, 77, 128, 16, True),
 ]
 
 
-@pytest.mark.parametrize("tiles", [1, 2])
+@pytest.mark.parametrize("tiles", [1, 2, 3])
 @pytest.mark.parametrize("case", FWD_TILE_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_forward_tiles_per_cta(case, tiles):
-    """Both forward kernels (one or two 128-row query tiles per CTA) against
-    the oracle, element by element."""
+    """Every forward kernel mode (one 128-row query tile per CTA; two tiles
+    that are adjacent query blocks of one head; two tiles that are one query
+    block of two heads sharing a KV head) against the oracle, element by
+    element."""
     dtype, B, H, HKV, T, D, window, causal = case
     w = Workload(103, "tiles", dtype, B, H, HKV, T, D, window, causal, False, "normal")
     inp = make_inputs(w, seed=2000 + T + D + H + window, with_dO=False)
