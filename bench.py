@@ -43,10 +43,13 @@ KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
 # ------------------------------------------------------------------ counting
 
 def visible_pairs(w: Workload) -> float:
-    """Visible (query, key) pairs per head as the metric counts them."""
+    """Visible (query, key) pairs per head as the metric counts them: T^2/2
+    under causal masking (the metric's "halved"), T*W - W(W-1)/2 with a
+    causal window W < T, and the exact count without causal masking (a
+    window there only drops keys more than W-1 before the query)."""
     T, W = w.T, w.window
     if not w.causal:
-        return float(T) * (min(W, T) if W else T)
+        return float(T) * T - ((T - W) * (T - W + 1) / 2.0 if W and W < T else 0.0)
     if W and W < T:
         return float(T) * W - W * (W - 1) / 2.0
     return T * T / 2.0
@@ -246,7 +249,8 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"  # gloo in the host tests
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
