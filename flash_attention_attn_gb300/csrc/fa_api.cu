@@ -26,6 +26,14 @@ std::atomic<int> g_fwd_tiles{0};  // 0 = automatic
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Test hook: 1 = the next 16-bit forward launch, 2 = the next dK/dV launch,
+// 3 = the next dQ launch withholds its first tile loads; taken (and cleared)
+// by the launch it names.
+int take_stall(int kind) {
+  int expected = kind;
+  return g_inject_stall.compare_exchange_strong(expected, 0) ? 1 : 0;
+}
+
 // T: query rows, Tk: key rows (T for self-attention).
 int validate_shape(int B, int T, int Tk, int H, int HKV, int D, float scale, int causal, int window, int dtype) {
   if (B < 1 || T < 1 || Tk < 1 || H < 1 || HKV < 1 || D < 1) return FA_ERR_INVALID_ARG;
@@ -171,7 +179,7 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.err = static_cast<unsigned int*>(workspace);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = g_wait_ns.load();
-  p.inject_stall = g_inject_stall.exchange(0);
+  p.inject_stall = take_stall(1);
   p.f16 = dtype == FA_DTYPE_FP16;
   return status_of(fa::launch_fwd_bf16(tm, p, s));
 }
@@ -206,9 +214,10 @@ int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, co
 }
 
 fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, void* dQ, void* dK, void* dV,
-                         void* workspace, int dtype) {
+                         void* workspace, int dtype, int stall_kind) {
   fa::BwdParams p;
   p.s = s;
+  p.inject_stall = take_stall(stall_kind);
   p.LSE = LSE;
   p.Delta = delta;
   p.dQ = dQ;
@@ -248,7 +257,7 @@ int dkdv_impl(const void* Q, const void* K, const void* V, const float* LSE, con
                                               delta, static_cast<float*>(dK), static_cast<float*>(dV), shp, s));
   fa::TensorMaps tm;
   if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
-  return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace, dtype), s));
+  return status_of(fa::launch_bwd_dkdv_bf16(tm, bwd_params(shp, LSE, delta, nullptr, dK, dV, workspace, dtype, 2), s));
 }
 
 int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
@@ -267,7 +276,7 @@ int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const
                                             static_cast<float*>(dQ), shp, s));
   fa::TensorMaps tm;
   if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
-  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype), s));
+  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype, 3), s));
 }
 
 int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
@@ -484,7 +493,8 @@ int fa_debug_fwd_tiles(int tiles) {
 
 int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall) {
   g_wait_ns.store(wait_timeout_ns ? wait_timeout_ns : fa::kDefaultWaitNs);
-  g_inject_stall.store(inject_stall ? 1 : 0);
+  if (inject_stall < 0 || inject_stall > 3) return FA_ERR_INVALID_ARG;
+  g_inject_stall.store(inject_stall);
   return FA_OK;
 }
 

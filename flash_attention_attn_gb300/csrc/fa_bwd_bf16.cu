@@ -230,10 +230,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, g, kb * BK, b);
-        tma_load_4d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, g, kb * BK, b);
+      if (!p.inject_stall) {
+        mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, g, kb * BK, b);
+          tma_load_4d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, g, kb * BK, b);
+        }
       }
     }
     // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n + 1 < niter) load_rows(n + 1);
     }
     if (lane == 0 && bars->abort) {
-      drain_bar(&bars->res_full, 0, p.timeout_ns);
+      if (!p.inject_stall) drain_bar(&bars->res_full, 0, p.timeout_ns);
       for (int n = imax(0, issued - C::kStages); n < issued; ++n)
         drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
     }
@@ -527,10 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
     }
-    mbar_arrive_expect_tx_e(&bars->res_full, 2 * C::kTile);
-    for (int c = 0; c < C::kChunks; ++c) {
-      tma_load_4d_e(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
-      tma_load_4d_e(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
+    if (!p.inject_stall) {
+      mbar_arrive_expect_tx_e(&bars->res_full, 2 * C::kTile);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d_e(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
+        tma_load_4d_e(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
+      }
     }
     int issued_k = 0, issued_v = 0;
     for (int n = 0; n < nblk; ++n) {
@@ -550,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       issued_v = n + 1;
     }
     if (bars->abort) {
-      drain_bar(&bars->res_full, 0, p.timeout_ns);
+      if (!p.inject_stall) drain_bar(&bars->res_full, 0, p.timeout_ns);
       for (int n = imax(0, issued_k - C::kKStages); n < issued_k; ++n)
         drain_bar(&bars->x_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
       for (int n = imax(0, issued_v - C::kVStages); n < issued_v; ++n)

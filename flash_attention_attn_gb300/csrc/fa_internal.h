@@ -95,6 +95,7 @@ struct FwdParams {
 
 struct BwdParams {
   Shape s;
+  int inject_stall;   // test hook: withhold the resident tile loads (the kernel's waits run out)
   const float* LSE;   // [B,H,T]
   const float* Delta; // [B,H,T]
   void* dQ;           // bf16 [B,T,H,D]

@@ -303,11 +303,12 @@ int fa_tile_n(void);
 
 /*
  * Test hook.  wait_timeout_ns: budget of one pipeline wait inside a kernel
- * (0 = the default of 2 s).  inject_stall: if nonzero, the next fa_fwd
- * launch of the bf16 forward withholds one tile load, so that the kernel's
- * wait runs out of budget and it exits with the device error word set; the
- * hook clears itself after that launch.  Affects later calls of this
- * process only.
+ * (0 = the default of 2 s).  inject_stall: 0 = none; 1, 2 or 3 = the next
+ * launch of the 16-bit forward, dK/dV or dQ kernel withholds its first tile
+ * loads, so that the kernel's waits run out of budget and it exits with the
+ * device error word set (FA_DEVERR_FWD_TIMEOUT, _DKDV_ or _DQ_); the hook
+ * clears itself at that launch.  FA_ERR_INVALID_ARG for other values.
+ * Affects later calls of this process only.
  */
 int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall);
 

@@ -1,9 +1,10 @@
 """Bounded waits: a kernel whose pipeline wait runs out of budget reports it
 through the device error word and leaves the context usable.
 
-The test hook makes the next bf16 forward launch withhold its tile loads (a
-barrier that nothing completes), with a 0.2 s wait budget.  No fault, trap or
-unbounded spin is involved: the kernel's own timer ends every wait.
+The test hook makes the next launch of one kernel (the 16-bit forward, dK/dV
+or dQ) withhold its first tile loads (a barrier that nothing completes), with
+a 0.2 s wait budget.  No fault, trap or unbounded spin is involved: the
+kernel's own timer ends every wait.
 """
 from __future__ import annotations
 
@@ -41,3 +42,38 @@ def test_stalled_forward_times_out_and_recovers():
     O, L = oracle.fwd(as_f64(inp["q"]), as_f64(inp["k"]), as_f64(inp["v"]), w.scale, True, 0)
     assert np.max(np.abs(o.float().cpu().numpy() - O)) <= 2e-2
     assert np.max(np.abs(lse.cpu().numpy() - L)) <= 1e-3
+
+
+@pytest.mark.parametrize("kind,bit", [(2, 2), (3, 4)], ids=["dkdv", "dq"])
+def test_stalled_backward_kernel_times_out_and_recovers(kind, bit):
+    from flash_attention_attn_gb300.build import build
+    build()
+    w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, 64, 0, True, True, "normal")
+    inp = make_inputs(w, seed=4)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    fa.check_status()
+    try:
+        fa.fa_debug_config(200_000_000, kind)
+        fa.attention_bwd(q, k, v, o, lse, do, causal=True)
+        st, word = fa.check_status()
+    finally:
+        fa.fa_debug_config(0, 0)
+    assert st == fa.FA_ERR_TIMEOUT
+    assert word & bit and not word & ~bit & 7, hex(word)  # only the stalled kernel reports
+    # the context still works and the next backward is correct
+    dq, dk, dv = fa.attention_bwd(q, k, v, o, lse, do, causal=True)
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, hex(word)
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, True, 0)
+    for got, ref in ((dq, dQ), (dk, dK), (dv, dV)):
+        g = got.float().cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 2e-2
+
+
+def test_stall_hook_rejects_unknown_kinds():
+    assert fa.fa_debug_config(0, 4) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_config(0, -1) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_config(0, 0) == fa.FA_OK
