@@ -280,10 +280,27 @@ def measure_prologue(w: Workload, dev, reps: int = 10):
     out = {}
     elem = qk.element_size()
     fbytes = 2 * f1.numel() * 4
+    # the two options need as many query as key heads: HKV of each, same
+    # tokens; paired heads take factor rows twice as wide, the key offset a
+    # half-width rotary part (its re-read of the previous token's key row is
+    # not counted: it is the same data)
+    h2 = max(2, w.HKV - (w.HKV % 2))
+    qk2 = torch.randn((tokens, 2 * h2, w.D), generator=gen, device=dev).to(dt)
+    f1p, f2p = torch.cat([f1, f1], dim=1).contiguous(), torch.cat([f2, f2], dim=1).contiguous()
+    opt_bytes = (2 * qk2.numel()) * elem  # read qk2, write q and k
+    g2 = torch.randn((tokens, h2, w.D), generator=gen, device=dev).to(dt)  # gradients of q and k
+    g2p = g2.reshape(2 * tokens, h2 // 2, w.D)
     for name, fn, nbytes in (
             ("fwd", lambda: fa.qk_norm_rope_fwd(qk, f1, f2, w.H, q=q, k=k), (qk.numel() + q.numel() + k.numel()) * elem + fbytes),
             ("bwd", lambda: fa.qk_norm_rope_bwd(dq, dk, qk, f1, f2, dqk=dqk),
-             (dq.numel() + dk.numel() + qk.numel() + dqk.numel()) * elem + fbytes)):
+             (dq.numel() + dk.numel() + qk.numel() + dqk.numel()) * elem + fbytes),
+            ("paired_fwd", lambda: fa.qk_norm_rope_fwd_opt(qk2, f1p, f2p, h2, 0, True, False), opt_bytes + 2 * fbytes),
+            ("key_offset_fwd", lambda: fa.qk_norm_rope_fwd_opt(qk2, f1, f2, h2, w.D // 2, False, True),
+             opt_bytes + fbytes),
+            ("paired_bwd", lambda: fa.qk_norm_rope_bwd_opt(g2p, g2p, qk2, f1p, f2p, h2, 0, True, False),
+             opt_bytes + qk2.numel() * elem + 2 * fbytes),
+            ("key_offset_bwd", lambda: fa.qk_norm_rope_bwd_opt(g2, g2, qk2, f1, f2, h2, w.D // 2, False, True),
+             opt_bytes + qk2.numel() * elem + fbytes)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize(dev)
