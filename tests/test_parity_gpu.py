@@ -238,6 +238,26 @@ def test_cross_attention_elementwise(case):
     check_grad(w, "dV", got["dv"], dV)
 
 
+def _random_cross_cases(n=12, seed=2027):
+    """Seeded random cross-attention shapes: dtype, batch, GQA ratio, query
+    and key lengths from 1 to 900 (ragged on both sides), head dims 16-128."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        hkv = int(rng.choice([1, 2, 4]))
+        h = hkv * int(rng.choice([1, 2, 3, 4]))
+        Tq, Tk = (int(x) for x in rng.integers(1, 900, size=2))
+        D = int(rng.choice([16, 32, 64, 80, 96, 128]))
+        dtype = str(rng.choice(["bf16", "fp16"]))
+        cases.append((dtype, int(rng.integers(1, 3)), h, hkv, Tq, Tk, D))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cross_cases(), ids=lambda c: "-".join(map(str, c)))
+def test_random_cross_shapes_elementwise(case):
+    test_cross_attention_elementwise(case)
+
+
 def test_cross_attention_rejects_masks():
     inp = make_cross_inputs("bf16", 1, 2, 2, 64, 96, 64, seed=1)
     dev = torch.device("cuda", 0)
