@@ -128,11 +128,11 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 namespace fa {
 int fwd_mode(const Shape& s) {
-  const bool heads_pair = (s.H / s.HKV) % 2 == 0;
   const int forced = g_fwd_tiles.load();
   if (forced == 1 || forced == 2) return forced;
-  if (heads_pair) return 3;
-  if (forced == 3) return ceil_div(s.T, kBM) >= 2 ? 2 : 1;
+  // automatic (0) and head pairs asked for (3): head pairs need an even
+  // number of query heads per KV head
+  if ((s.H / s.HKV) % 2 == 0) return 3;
   return ceil_div(s.T, kBM) >= 2 ? 2 : 1;
 }
 }  // namespace fa
