@@ -169,7 +169,7 @@ def test_forward_tiles_per_cta(case, tiles):
     check_fwd(w, got["o"], O, got["lse"], LSE)
 
 
-def _random_cases(n=16, seed=2026):
+def _random_cases(n=32, seed=2026):
     """Seeded random shapes across the supported space: dtype, batch, GQA
     ratio, ragged lengths, head dims 16..128, causal or not, windows."""
     rng = np.random.default_rng(seed)
@@ -238,7 +238,7 @@ def test_cross_attention_elementwise(case):
     check_grad(w, "dV", got["dv"], dV)
 
 
-def _random_cross_cases(n=12, seed=2027):
+def _random_cross_cases(n=20, seed=2027):
     """Seeded random cross-attention shapes: dtype, batch, GQA ratio, query
     and key lengths from 1 to 900 (ragged on both sides), head dims 16-128."""
     rng = np.random.default_rng(seed)
