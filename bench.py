@@ -596,6 +596,10 @@ def main():
         "fwd_pct_of_peak": 100.0 * flops["fwd"] / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
         "fwd_bwd_pct_of_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
         "fwd_bwd_tflops_x14": 14.0 / 10.0 * value,
+        # the other reading of "10*B*H*T^2*D": FlashAttention's count for the
+        # backward alone, over the three backward kernels' time
+        "bwd_only_tflops_x10": flops["fwd_bwd"] / (sum(statistics.mean(r["per_kernel_ms"][n])
+                                                     for n in KERNELS if n != "fwd") / 1e3) / 1e12,
         "peak_bf16_tflops": peaks["bf16_tflops_sustained"],
         "peak_source": peak_src,
         "roofline": roof,
