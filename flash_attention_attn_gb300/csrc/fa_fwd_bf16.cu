@@ -1,8 +1,12 @@
 // fa_fwd_bf16.cu -- fused causal / sliding-window GQA attention forward for
 // sm_103a: TMA -> shared memory -> tcgen05 MMA -> TMEM, online softmax in
-// registers.
+// registers.  Two kernels: the two-tile kernel further down (two 128-row
+// query tiles per CTA, used for almost every shape) and, first, the one-tile
+// kernel (sequences of one query tile with an odd number of query heads per
+// KV head, and the test hook).
 //
-// One CTA computes one 128-row query tile of one (b, h).  Warp roles:
+// One-tile kernel: one CTA computes one 128-row query tile of one (b, h).
+// Warp roles:
 //   warps 0-3  softmax: thread t owns query row t of the tile (= TMEM lane t).
 //   warp  4    TMA producer: the Q tile once, then K and V blocks through an
 //              NS-stage ring guarded by full/empty mbarriers (a K stage is
@@ -354,17 +358,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- two tiles
 //
-// Two 128-row query tiles A and B (query blocks 2j and 2j + 1) of one (b, h)
-// per CTA, sharing every K/V block the CTA streams: each 64 KB K/V block
+// Two 128-row query tiles A and B per CTA, sharing every K/V block the CTA
+// streams: one query block of two query heads that share a KV head (head
+// pairs, when H/HKV is even; both tiles see the same key range) or query
+// blocks 2j and 2j + 1 of one head (block pairs).  Each 64 KB K/V block
 // (D = 128) feeds four 128x128 MMA groups instead of two, which halves the
 // TMA traffic per MMA.  Measured on GB300, a K/V ring feeding one tile is
 // bounded near 1600 cycles per block by the TMA stream itself against 1024
 // cycles of MMAs.
 //   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B (warp w owns
 //             TMEM lanes 32*(w%4).. = rows of its tile)
-//   warp  8   TMA (lane 0): Q_A, Q_B, then K and V blocks in the order the
+//   warp  8   TMA producer: Q_A, Q_B, then K and V blocks in the order the
 //             MMAs need them
-//   warp  9   MMA issuer (lane 0) and TMEM owner
+//   warp  9   MMA issuer and TMEM owner
+// (both run converged; one elected lane issues each copy and each MMA)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
 // No S buffer is doubled; the tiles ping-pong instead.  Per streamed block n
 // the MMA queue is  PV_A(n) S_A(n+1) PV_B(n) S_B(n+1), so the softmax of one
