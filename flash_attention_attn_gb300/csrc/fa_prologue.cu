@@ -3,9 +3,10 @@
 // and K tensors the attention forward reads; and its backward.
 //
 // What it computes is the modded-nanogpt page qkv_rope.py (module docstring
-// and `_qk_norm_rope_forward_kernel`, without its paired-heads and key-offset
-// options; the backward is the norm/rotary part of
-// `_qkv_norm_rope_pack_fp8_backward_kernel` without the fp8 packing):
+// and `_qk_norm_rope_forward_kernel`; the backward is the norm/rotary part of
+// `_qkv_norm_rope_pack_fp8_backward_kernel` without the fp8 packing).  The
+// plain kernels below take any hq, hk; the page's paired-heads and
+// key-offset options have their own kernels further down:
 //
 //   x = qk[t][c][:]            (c < hq: query head c, else key head c - hq)
 //   rstd = 1 / sqrt(mean_d x_d^2 + 2^-23),  n = rstd x
