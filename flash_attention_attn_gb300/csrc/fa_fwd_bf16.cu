@@ -638,26 +638,20 @@ __global__ void __launch_bounds__(kThreads2, 1)
       // One TMEM round trip per block: the row's 128 scores stay in registers
       // for both passes (re-reading them for pass 2 cost two more load
       // latencies on the softmax's critical path).
+      // pass 1 rides on the loads: each 32-column load also returns the
+      // maximum of its values (sm_103a load-with-reduction)
       uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(s_addr, s0);
-      tmem_ld32(s_addr + 32, s1);
-      tmem_ld32(s_addr + 64, s2);
-      tmem_ld32(s_addr + 96, s3);
+      float m0, m1, m2, m3;
+      tmem_ld32_max(s_addr, s0, m0);
+      tmem_ld32_max(s_addr + 32, s1, m1);
+      tmem_ld32_max(s_addr + 64, s2, m2);
+      tmem_ld32_max(s_addr + 96, s3, m3);
       tmem_ld_wait(s0);
       reg_tie(s1);
       reg_tie(s2);
       reg_tie(s3);
-      // pass 1: row max over eight independent partials
-      float mx8[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        mx8[c & 7] = fmax3(mx8[c & 7], __uint_as_float(s0[c]), __uint_as_float(s1[c]));
-        mx8[(c + 4) & 7] = fmax3(mx8[(c + 4) & 7], __uint_as_float(s2[c]), __uint_as_float(s3[c]));
-      }
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      reg_tie4(m0, m1, m2, m3);
+      float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
       mx *= sl2;  // scale > 0, so the max commutes with the scaling
       const float m_new = fmaxf(m_run, mx);
       const bool first = (j == 0);
