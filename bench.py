@@ -464,7 +464,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
             barrier(world)
             return max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
 
-        e2e_steps = max(3, min(K, 6))
+        e2e_steps = max(3, min(K, 10))  # the pipeline fills and drains once per measurement
         timed(True, 2)  # warm the copy path and the second buffer set
         e2e_s = timed(True, e2e_steps)
         serial_s = timed(False, e2e_steps)
