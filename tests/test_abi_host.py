@@ -247,3 +247,47 @@ def test_masked_causal_blocks_follow_triu_offsets(lib, BM, BN):
 
 def test_tile_sizes(lib):
     assert fb.fa_tile_m() == 128 and fb.fa_tile_n() == 128
+
+
+# ------------------------------------------------ randomised planner checks
+
+def test_planner_properties_on_random_shapes(lib):
+    """Random (Tq = Tk = T, tile sizes, causal, window): every visible element
+    lies in a visited block, every block outside the visited range is wholly
+    masked, and a block flagged mask-free has no masked element (the
+    properties the kernels rely on; hypothesis when installed, else a seeded
+    sample)."""
+    def check(T, BM, BN, causal, W):
+        vis = visible(T, causal, W)
+        nq, nk = -(-T // BM), -(-T // BN)
+        for qb in range(nq):
+            lo, hi = fb.fa_plan_kv_range(T, BM, BN, causal, W, qb)
+            rows = vis[qb * BM:(qb + 1) * BM]
+            for kb in range(nk):
+                blk = rows[:, kb * BN:(kb + 1) * BN]
+                if not (lo <= kb <= hi):
+                    assert not blk.any(), (T, BM, BN, causal, W, qb, kb)
+                elif fb.fa_plan_block_mask(T, BM, BN, causal, W, qb, kb) == 0:
+                    assert blk.shape == (BM, BN) and blk.all(), (T, BM, BN, causal, W, qb, kb)
+        for kb in range(nk):
+            lo, hi = fb.fa_plan_q_range(T, BM, BN, causal, W, kb)
+            for qb in range(nq):
+                if not (lo <= qb <= hi):
+                    assert not vis[qb * BM:(qb + 1) * BM, kb * BN:(kb + 1) * BN].any()
+
+    try:
+        from hypothesis import given, settings, strategies as st
+    except ImportError:
+        rng = np.random.default_rng(7)
+        for _ in range(200):
+            check(int(rng.integers(1, 400)), int(rng.integers(1, 130)), int(rng.integers(1, 130)),
+                  int(rng.integers(0, 2)), int(rng.choice([0, 0, 1, int(rng.integers(1, 500))])))
+        return
+
+    @settings(max_examples=300, deadline=None)
+    @given(st.integers(1, 400), st.integers(1, 130), st.integers(1, 130), st.integers(0, 1),
+           st.one_of(st.just(0), st.integers(1, 500)))
+    def run(T, BM, BN, causal, W):
+        check(T, BM, BN, causal, W)
+
+    run()
