@@ -140,7 +140,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -315,6 +315,149 @@ def measure_prologue(w: Workload, dev, reps: int = 10):
     return out
 
 
+class _Sets:
+    """Device buffers of one workload, `n` independent sets of inputs and
+    outputs: consecutive timed iterations use different sets, so that with
+    enough sets the loop's working set exceeds L2 and every iteration reads
+    its inputs from HBM."""
+
+    def __init__(self, w: Workload, dev, n: int, lib, fb):
+        import torch
+        self.w, self.lib, self.fb = w, lib, fb
+        self.dt = {"bf16": fb.FA_DTYPE_BF16, "fp16": fb.FA_DTYPE_FP16, "fp32": fb.FA_DTYPE_FP32}[w.dtype]
+        inp = make_inputs(w, seed=w.wid, with_dO=w.bwd)
+        self.ws_bytes = fb.fa_workspace_size(fb.FA_OP_BWD, w.B, w.T, w.H, w.HKV, w.D, self.dt)
+        self.sets = []
+        for _ in range(n):
+            q, k, v = (inp[x].to(dev) for x in ("q", "k", "v"))
+            do = inp["do"].to(dev) if w.bwd else q
+            o = torch.empty_like(q)
+            lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+            dq, dk, dv = (torch.empty_like(t) for t in (q, k, v)) if w.bwd else (q, k, v)
+            ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
+            self.sets.append((q, k, v, o, lse, do, dq, dk, dv, ws))
+        self.stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def stage(self, name: str, i: int):
+        w, lib, fb = self.w, self.lib, self.fb
+        q, k, v, o, lse, do, dq, dk, dv, ws = (t.data_ptr() for t in self.sets[i % len(self.sets)])
+        a = (w.B, w.T, w.H, w.HKV, w.D)
+        sc, c, win, dt, n, s = float(w.scale), int(w.causal), int(w.window), self.dt, self.ws_bytes, self.stream
+        if name == "fwd":
+            st = lib.fa_fwd(q, k, v, o, lse, *a, sc, c, win, dt, ws, n, s)
+        elif name == "bwd_preprocess":
+            st = lib.fa_bwd_preprocess(o, do, *a, dt, ws, n, s)
+        elif name == "bwd_dkdv":
+            st = lib.fa_bwd_dkdv(q, k, v, lse, do, dk, dv, *a, sc, c, win, dt, ws, n, s)
+        else:
+            st = lib.fa_bwd_dq(q, k, v, lse, do, dq, *a, sc, c, win, dt, ws, n, s)
+        if st != 0:
+            raise fb.FaError(st, name)
+
+    def check(self):
+        for t in self.sets:
+            st, word = self.fb.fa_check_status(t[-1].data_ptr(), self.stream)
+            if st != 0:
+                raise RuntimeError(f"device error word {word:#x}")
+
+
+def _loop_ms(fn, steps: int, stream) -> float:
+    """Device time of `steps` back-to-back calls of fn(i), two CUDA events
+    on the launching stream around the whole loop, per call."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def measure_workload(w: Workload, dev, peaks: dict, min_loop_ms: float = 200.0, repeats: int = 5,
+                     kernel_loop_ms: float = 100.0) -> dict:
+    """Throughput of one workload at its full size, timed the way short
+    kernels need: each timed loop runs at least min_loop_ms of back-to-back
+    steps (the step count comes from a calibration pass) and the step time is
+    the median over `repeats` such loops; each kernel is also timed alone in
+    loops of at least kernel_loop_ms (median of 3).  The loop cycles through
+    enough input sets that its working set is more than twice L2; the clock
+    sampler runs over the whole measurement."""
+    import torch
+    import flash_attention_attn_gb300 as fa
+    from flash_attention_attn_gb300 import _binding as fb
+
+    lib = fa.load()
+    elem = {"bf16": 2, "fp16": 2, "fp32": 4}[w.dtype]
+    set_bytes = w.B * w.T * (w.H * (2 if w.bwd else 1) + 2 * w.HKV) * w.D * elem
+    n_sets = max(1, min(2048, math.ceil(2 * L2_BYTES / set_bytes)))
+    sets = _Sets(w, dev, n_sets, lib, fb)
+    stages = ["fwd"] + (["bwd_preprocess", "bwd_dkdv", "bwd_dq"] if w.bwd else [])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        for name in stages:
+            sets.stage(name, i)
+
+    for i in range(max(3, n_sets)):  # warm-up: every set gets a valid O, LSE and Delta
+        step(i)
+    torch.cuda.synchronize(dev)
+    sets.check()
+    est = _loop_ms(step, max(3, min(n_sets, 50)), stream)
+    steps = max(n_sets, int(math.ceil(min_loop_ms / max(est, 1e-3))))
+    with ClockSampler(dev.index or 0) as clocks:
+        loops = [_loop_ms(step, steps, stream) for _ in range(repeats)]
+        kern = {}
+        for name in stages:
+            f = (lambda nm: (lambda i: sets.stage(nm, i)))(name)
+            one = _loop_ms(f, max(3, min(n_sets, 50)), stream)
+            ksteps = max(n_sets, int(math.ceil(kernel_loop_ms / max(one, 1e-3))))
+            kern[name] = statistics.median(_loop_ms(f, ksteps, stream) for _ in range(3))
+    sets.check()
+    step_ms = statistics.median(loops)
+    flops = counted_flops(w)
+    work = kernel_work(w, elem)
+    burst, sust = peaks["bf16_tflops"], peaks["bf16_tflops_sustained"]
+    tensor = w.dtype in ("bf16", "fp16")
+    out = {"workload": w.name, "dtype": w.dtype, "B": w.B, "H": w.H, "HKV": w.HKV, "T": w.T, "head_dim": w.D,
+           "window": w.window, "causal": w.causal, "steps_per_loop": steps, "loops": repeats,
+           "loop_ms": [ms * steps for ms in loops], "step_ms": step_ms,
+           "l2": (f"{n_sets} rotating input sets, {n_sets * set_bytes / 2**20:.0f} MiB of inputs per pass "
+                  f"(more than twice L2), no flush"),
+           "clocks": clocks.summary()}
+    fwd_ms = kern["fwd"]
+    out["fwd_ms"] = fwd_ms
+    out["fwd_tflops"] = flops["fwd"] / (fwd_ms / 1e3) / 1e12
+    if w.bwd:
+        out["fwd_bwd_ms"] = step_ms
+        out["fwd_bwd_tflops"] = flops["fwd_bwd"] / (step_ms / 1e3) / 1e12
+    if tensor:
+        out["fwd_pct_of_burst"] = 100.0 * out["fwd_tflops"] / burst
+        out["fwd_pct_of_sustained"] = 100.0 * out["fwd_tflops"] / sust
+        if w.bwd:
+            out["fwd_bwd_pct_of_burst"] = 100.0 * out["fwd_bwd_tflops"] / burst
+            out["fwd_bwd_pct_of_sustained"] = 100.0 * out["fwd_bwd_tflops"] / sust
+    else:
+        out["note"] = "fp32 CUDA-core kernels (correctness workload); no tensor-peak target"
+    out["kernels"] = {}
+    for name in stages:
+        bound, amount = work[name]
+        ms = kern[name]
+        if bound == "tensor":
+            ach = amount / (ms / 1e3) / 1e12
+            k = {"ms": ms, "achieved": ach, "unit": "TFLOP/s"}
+            if tensor:
+                k.update(frac_of_burst=ach / burst, frac_of_sustained=ach / sust)
+        else:
+            ach = amount / (ms / 1e3) / 1e9
+            k = {"ms": ms, "achieved": ach, "unit": "GB/s", "frac": ach / peaks["hbm_gbs"]}
+        out["kernels"][name] = k
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
     import torch
     import flash_attention_attn_gb300 as fa
@@ -416,49 +559,63 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
                   "fa_bwd_dq")
 
         def timed(pipelined, steps):
-            cs = torch.cuda.Stream(dev)
-            done = [torch.cuda.Event() for _ in range(2)]  # compute of the set finished
+            # Uploads and downloads run on streams of their own, so that the two
+            # directions of the host link work at the same time.  Set i % 2
+            # serves step i; its inputs may be overwritten once the compute of
+            # step i - 2 is done, its outputs once their download is done.
+            cs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+            done = [None, None]     # compute of the set's last step finished
+            fetched = [None, None]  # outputs of the set's last step copied out
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             barrier(world)
             torch.cuda.synchronize(dev)
             e0.record(stream)
-            cs.wait_event(e0)
 
-            def upload(i):  # inputs of step i into set i % 2, on the copy stream
+            def mark(st):
+                ev = torch.cuda.Event()
+                ev.record(st)
+                return ev
+
+            def upload(i, after):  # inputs of step i into set i % 2, on the upload stream
+                cs.wait_event(after)
+                if done[i % 2] is not None:
+                    cs.wait_event(done[i % 2])
                 with torch.cuda.stream(cs):
                     for hsrc, ddst in zip(h_in, sets[i % 2][:4]):
                         ddst.copy_(hsrc, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(cs)
-                return ev
+                return mark(cs)
+
+            def compute(i, ready):
+                stream.wait_event(ready)
+                if fetched[i % 2] is not None:
+                    stream.wait_event(fetched[i % 2])
+                run_set(sets[i % 2])
+                done[i % 2] = mark(stream)
 
             def download(i):  # results of step i, once its compute is done
-                cs.wait_event(done[i % 2])
-                with torch.cuda.stream(cs):
+                ds.wait_event(done[i % 2])
+                with torch.cuda.stream(ds):
                     for dsrc, hdst in zip(sets[i % 2][4:], h_out):
                         hdst.copy_(dsrc, non_blocking=True)
+                fetched[i % 2] = mark(ds)
 
             if pipelined:
-                ready = upload(0)
+                # step i + 1's inputs go up and step i - 1's results come down
+                # while step i computes
+                ready = upload(0, e0)
                 for i in range(steps):
-                    stream.wait_event(ready)
-                    if i + 1 < steps:
-                        ready = upload(i + 1)  # set (i+1)%2: its last reader, step i-1, is ordered before on cs
-                    run_set(sets[i % 2])
-                    done[i % 2].record(stream)
+                    nxt = upload(i + 1, e0) if i + 1 < steps else None
+                    compute(i, ready)
                     download(i)
+                    ready = nxt
             else:
+                # copy in, compute, copy out, one after the other
+                after = e0
                 for i in range(steps):
-                    stream.wait_event(upload(i))
-                    run_set(sets[i % 2])
-                    done[i % 2].record(stream)
+                    compute(i, upload(i, after))
                     download(i)
-                    tail = torch.cuda.Event()
-                    tail.record(cs)
-                    stream.wait_event(tail)
-            tail = torch.cuda.Event()
-            tail.record(cs)
-            stream.wait_event(tail)
+                    after = fetched[i % 2]
+            stream.wait_event(fetched[(steps - 1) % 2])
             e1.record(stream)
             torch.cuda.synchronize(dev)
             barrier(world)
@@ -478,7 +635,11 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
                "serial": {"value": flops / serial_s / 1e12, "ms_per_step": 1e3 * serial_s / e2e_steps}}
 
     prologue = None if args.no_prologue else measure_prologue(w, dev)
-    return {"per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
+    side = None
+    if not args.no_workloads and world == 1:
+        peaks, _ = load_peaks()
+        side = {str(i): measure_workload(WORKLOADS[i], dev, peaks) for i in sorted(WORKLOADS) if i != w.wid}
+    return {"workloads": side, "per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
             "e2e": e2e, "elem_bytes": q.element_size(), "prologue": prologue}
 
 
@@ -511,6 +672,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue", action="store_true", help="skip the QK-norm + rotary prologue measurement")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the other configurations' loops")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.shape:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -559,7 +721,7 @@ def main():
         ms = statistics.mean(r["per_kernel_ms"][name])
         bound, amount = work[name]
         if bound == "tensor":
-            peak = peaks["bf16_tflops_sustained"]
+            peak = peaks["bf16_tflops"]
             achieved = amount / (ms / 1e3) / 1e12
             unit = "TFLOP/s"
         else:
@@ -568,12 +730,16 @@ def main():
             unit = "GB/s"
         kern[name] = {"ms": ms, "bound": bound, "achieved": achieved, "unit": unit, "peak": peak,
                       "frac": achieved / peak, "work_per_launch": amount}
+        if bound == "tensor":
+            kern[name]["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
     dom = max(KERNELS, key=lambda n: kern[n]["ms"])
     traffic = ncu_traffic(dom, w.name)
     roof = {"bound": kern[dom]["bound"], "achieved": kern[dom]["achieved"], "peak": kern[dom]["peak"],
             "unit": kern[dom]["unit"], "frac": kern[dom]["frac"], "traffic": traffic, "kernel": dom,
             "work_per_launch": kern[dom]["work_per_launch"],
-            "peak_source": f"{peak_src} ({'sustained bf16' if kern[dom]['bound'] == 'tensor' else 'HBM copy'})"}
+            "peak_source": f"{peak_src} ({'burst cuBLAS bf16' if kern[dom]['bound'] == 'tensor' else 'HBM copy'})"}
+    if kern[dom]["bound"] == "tensor":
+        roof["frac_of_sustained"] = kern[dom]["frac_of_sustained"]
     fwd_ms = statistics.mean(r["per_kernel_ms"]["fwd"])
     in_bytes = w.B * w.T * (2 * w.H + 2 * w.HKV) * w.D * r["elem_bytes"]
     l2_note = ("inputs larger than L2 (no flush)" if in_bytes > L2_BYTES
@@ -593,15 +759,19 @@ def main():
         "data": "synthetic",
         "config": config_of(w, l2_note),
         "fwd_tflops": flops["fwd"] / (fwd_ms / 1e3) / 1e12,
-        "fwd_pct_of_peak": 100.0 * flops["fwd"] / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
-        "fwd_bwd_pct_of_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+        "fwd_pct_of_peak": 100.0 * flops["fwd"] / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+        "fwd_bwd_pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
+        "fwd_pct_of_sustained": 100.0 * flops["fwd"] / (fwd_ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "fwd_bwd_pct_of_sustained": 100.0 * value / world / peaks["bf16_tflops_sustained"],
         "fwd_bwd_tflops_x14": 14.0 / 10.0 * value,
         # the other reading of "10*B*H*T^2*D": FlashAttention's count for the
         # backward alone, over the three backward kernels' time
         "bwd_only_tflops_x10": flops["fwd_bwd"] / (sum(statistics.mean(r["per_kernel_ms"][n])
                                                      for n in KERNELS if n != "fwd") / 1e3) / 1e12,
-        "peak_bf16_tflops": peaks["bf16_tflops_sustained"],
-        "peak_source": peak_src,
+        "peak_bf16_tflops": peaks["bf16_tflops"],
+        "peak_bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
+        "peak_source": f"{peak_src}: pct_of_peak against the burst cuBLAS bf16 rate, _of_sustained against the "
+                       "seconds-long loop under the power cap",
         "roofline": roof,
         "kernels": kern,
         "gpu_launches": 4 * args.steps,
@@ -613,6 +783,10 @@ def main():
         # outside the timed step: the QK-norm + rotary prologue on the same shape (HBM-bound)
         line["prologue"] = {n: dict(v, peak_gbs=peaks["hbm_gbs"], frac=v["achieved_gbs"] / peaks["hbm_gbs"])
                             for n, v in r["prologue"].items()}
+    if r["workloads"]:
+        # the other configurations, each in its own >= 200 ms loops (median of 5)
+        line["workloads"] = r["workloads"]
+        line["gpu_launches_workloads"] = "outside the timed steps; not counted in gpu_launches"
     if cpu is not None:
         t = cpu["seconds"][0]
         line["cpu_baseline"] = {

@@ -202,6 +202,22 @@ int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int Tk, int H,
   return FA_OK;
 }
 
+}  // namespace
+
+namespace fa {
+int check_bwd_call(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                   void* dQ, void* dK, void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal,
+                   int window, int dtype, void* workspace, size_t workspace_bytes) {
+  const void* ptrs[] = {Q, K, V, O, LSE, dO, dQ, dK, dV};
+  Shape shp;
+  float* delta;
+  return bwd_prologue(ptrs, 9, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace, workspace_bytes,
+                      &shp, &delta);
+}
+}  // namespace fa
+
+namespace {
+
 int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, const void* dO, const Shape& s,
              int dtype) {
   int st;

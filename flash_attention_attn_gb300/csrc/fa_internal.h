@@ -136,6 +136,13 @@ int fwd_mode(const Shape& s);
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 
+// Every host-side check fa_bwd makes (shape, pointers and their alignment,
+// workspace size and alignment, device) without launching anything: FA_OK or
+// the status fa_bwd would return for the same arguments.
+int check_bwd_call(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO,
+                   void* dQ, void* dK, void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal,
+                   int window, int dtype, void* workspace, size_t workspace_bytes);
+
 // ---------------------------------------------------------- shared kernels
 
 // Delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d], fp32 accumulation.

@@ -177,14 +177,21 @@ int fa_bwd_cross(const void* Q, const void* K, const void* V, const void* O, con
  *     FA_ERR_WORKSPACE before anything is launched.
  *   err_word: optional caller-owned device pointer (4-byte aligned) that
  *     receives this call's device error word (0, or fa_device_error_bits
- *     when a kernel wait ran out of budget); NULL to skip.
+ *     when a kernel wait ran out of budget).  With NULL the word stays
+ *     inside the library, where no caller can read it: a kernel that gave
+ *     up on a wait then goes unreported and dQ, dK and dV may be partly
+ *     unwritten.  Pass a word whenever the outputs matter.
  *   No allocation: the call makes no cudaMalloc/cudaFree or other allocating
  *     call; it only issues a 4-byte memset (clearing the error word, since
  *     the array keeps the previous call's contents), the three backward
  *     kernels, and, with err_word, a 4-byte device-to-device copy.
+ *   Validation: every check of fa_bwd runs before anything is queued, so a
+ *     call that fails it launches nothing.
  *   Set-up: the first call on each device looks the array's device address
  *     up with that device current (cudaGetSymbolAddress); make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is cached per device and
+ *     context: after cudaDeviceReset (a new context, in which the array is
+ *     loaded again) the next call looks it up afresh.
  *   Sharing: all calls share the one array per device, so calls whose work
  *     overlaps on the GPU (different streams, or threads racing on one
  *     device) race on it; order them on one stream.

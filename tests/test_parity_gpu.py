@@ -308,9 +308,18 @@ def _sample_rows(T, rng, n_random):
 def _dkdv_sample(w: Workload, rng):
     if w.window > 0 or w.T <= 2048:
         return _sample_rows(w.T, rng, 12)
-    # under plain causal masking key row j is seen by rows j..T-1: keep to the
-    # last 256 keys so that each row's statistics stay cheap for the oracle
-    return sorted(set([w.T - 1, w.T - 2, w.T - 129, w.T - 256] + rng.integers(w.T - 256, w.T, size=8).tolist()))
+    # Plain causal masking over a long sequence: key j is seen by query rows
+    # j..T-1 of every head of its group (forge flash_attn_bwd_dk / _dv, query
+    # range starting at j), so the early keys carry the longest accumulations
+    # and key 0 sums over every query row.  Take those keys, the ones either
+    # side of the first block edge and of the middle, the last keys, and
+    # random keys over the whole range.  With key 0 in the set the oracle
+    # evaluates every query row of the group once (about 1.1e12 fp64 flops
+    # per KV head at T = 32768).
+    T = w.T
+    fixed = {0, 1, 127, 128, 129, T // 2, T // 2 + 1, T - 256, T - 129, T - 2, T - 1}
+    rnd = rng.integers(0, T, size=8).tolist() + rng.integers(T - 256, T, size=4).tolist()
+    return sorted(fixed | set(rnd))
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
