@@ -136,12 +136,24 @@ class ClockSampler:
         self.path = os.path.join("/tmp", f"fa_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
+        self.skip = 0
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            # nvidia-smi takes a while to start: wait for its first sample so
+            # that the region is covered from its start, and drop the samples
+            # taken before it
+            t0 = time.time()
+            while time.time() - t0 < 20.0 and self.proc.poll() is None:
+                with open(self.path) as f:
+                    n = sum(1 for _ in f)
+                if n:
+                    self.skip = n
+                    break
+                time.sleep(0.02)
         except Exception:
             self.proc = None
         return self
@@ -160,7 +172,9 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
             with open(self.path) as f:
-                for line in f:
+                for k, line in enumerate(f):
+                    if k < self.skip:
+                        continue
                     cols = [c.strip() for c in line.split(",")]
                     if len(cols) < 8:
                         continue

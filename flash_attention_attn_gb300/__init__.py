@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     fa_check_status,
     fa_debug_config,
     fa_debug_fwd_tiles,
+    fa_debug_max_ctas,
     fa_fwd,
     fa_fwd_cross,
     fa_plan_block_mask,

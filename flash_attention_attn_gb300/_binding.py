@@ -98,6 +98,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_debug_config.restype = _i
         lib.fa_debug_fwd_tiles.argtypes = [_i]
         lib.fa_debug_fwd_tiles.restype = _i
+        lib.fa_debug_max_ctas.argtypes = [_i]
+        lib.fa_debug_max_ctas.restype = _i
         lib.fa_qk_norm_rope_fwd.argtypes = [_vp] * 5 + [_i] * 5 + [_vp]
         lib.fa_qk_norm_rope_fwd.restype = _i
         lib.fa_qk_norm_rope_bwd.argtypes = [_vp] * 6 + [_i] * 5 + [_vp]
@@ -219,6 +221,10 @@ def fa_debug_config(wait_timeout_ns: int = 0, inject_stall: int = 0) -> int:
 
 def fa_debug_fwd_tiles(tiles: int = 0) -> int:
     return load().fa_debug_fwd_tiles(int(tiles))
+
+
+def fa_debug_max_ctas(ctas: int = 0) -> int:
+    return load().fa_debug_max_ctas(int(ctas))
 
 
 def fa_qk_norm_rope_fwd(qk, f1, f2, q, k, tokens, hq, hk, head_dim, dtype, stream) -> int:

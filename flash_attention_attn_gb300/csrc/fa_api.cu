@@ -16,13 +16,22 @@ namespace {
 
 using fa::Shape;
 
-constexpr size_t kErrBytes = 256;  // error word, padded to keep Delta aligned
+// The workspace's first 256 bytes: the device error word at 0, the work
+// counters of the persistent kernels at kSchedOffset (forward, dK/dV, dQ;
+// 8 bytes each); then Delta.
+constexpr size_t kErrBytes = 256;
+constexpr size_t kSchedOffset = 64;
+
+fa::SchedCounter* sched_counter(void* workspace, int which) {
+  return reinterpret_cast<fa::SchedCounter*>(static_cast<char*>(workspace) + kSchedOffset + 8 * which);
+}
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 std::atomic<unsigned long long> g_wait_ns{fa::kDefaultWaitNs};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_fwd_tiles{0};  // 0 = automatic
+std::atomic<int> g_max_ctas{0};   // 0 = one CTA per SM
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -90,6 +99,14 @@ int device_ok(int* dev_out) {
   }
   *dev_out = dev;
   return d.sm103 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// CTAs of a persistent kernel on device `dev`: one per SM, or the number
+// the test hook sets (the launch takes at most one CTA per work unit).
+int persistent_ctas(int dev) {
+  const int cap = g_max_ctas.load();
+  const int sms = g_dev[dev].sms > 0 ? g_dev[dev].sms : 1;
+  return cap > 0 ? cap : sms;
 }
 
 int get_encoder() {
@@ -181,6 +198,8 @@ int fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, i
   p.timeout_ns = g_wait_ns.load();
   p.inject_stall = take_stall(1);
   p.f16 = dtype == FA_DTYPE_FP16;
+  p.ctas = persistent_ctas(dev);
+  p.sched = sched_counter(workspace, 0);
   return status_of(fa::launch_fwd_bf16(tm, p, s));
 }
 
@@ -232,6 +251,10 @@ int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, co
 fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, void* dQ, void* dK, void* dV,
                          void* workspace, int dtype, int stall_kind) {
   fa::BwdParams p;
+  int dev = 0;
+  cudaGetDevice(&dev);  // already checked by bwd_prologue
+  p.ctas = persistent_ctas(dev);
+  p.sched = sched_counter(workspace, stall_kind == 2 ? 1 : 2);  // the dK/dV or the dQ kernel's counter
   p.s = s;
   p.inject_stall = take_stall(stall_kind);
   p.LSE = LSE;
@@ -500,6 +523,12 @@ int fa_qk_norm_rope_bwd_opt(const void* dq, const void* dk, const void* qk, cons
 
 int fa_tile_m(void) { return fa::kBM; }
 int fa_tile_n(void) { return fa::kBN; }
+
+int fa_debug_max_ctas(int ctas) {
+  if (ctas < 0) return FA_ERR_INVALID_ARG;
+  g_max_ctas.store(ctas);
+  return FA_OK;
+}
 
 int fa_debug_fwd_tiles(int tiles) {
   if (tiles < 0 || tiles > 3) return FA_ERR_INVALID_ARG;

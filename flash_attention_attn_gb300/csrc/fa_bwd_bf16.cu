@@ -39,6 +39,7 @@
 #include <math_constants.h>
 
 #include "fa_internal.h"
+#include "fa_sched.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -101,6 +102,7 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, int nva
 
 struct BwdBars {
   uint64_t res_full;
+  uint64_t res_empty;  // the unit's MMAs are done with the resident tiles
   uint64_t x_full[kStages];   // streamed stage (K in dQ) loaded
   uint64_t x_empty[kStages];  // streamed stage (K in dQ) free
   uint64_t v_full[kStages];   // dQ only: V stage loaded
@@ -111,12 +113,16 @@ struct BwdBars {
   uint64_t ds_full[2];  // dS (and P) written back (256 compute threads)
   uint64_t acc_full;
   uint64_t drain;
+  SchedRing sched;  // units handed from the producer to the other roles
   uint32_t tmem_base;
   int abort;
 };
 
+static_assert(sizeof(BwdBars) <= 512, "backward barriers exceed their shared-memory slot");
+
 __device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) {
   mbar_init(&bars->res_full, 1);
+  mbar_init(&bars->res_empty, 1);
   for (int i = 0; i < kStages; ++i) {
     mbar_init(&bars->x_full[i], x_full_count);
     mbar_init(&bars->x_empty[i], 1);
@@ -131,6 +137,7 @@ __device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) 
   }
   mbar_init(&bars->acc_full, 1);
   mbar_init(&bars->drain, 1);
+  sched_init(&bars->sched, 9);  // consumers: eight compute warps and the MMA warp
   bars->abort = 0;
   fence_mbar_init();
 }
@@ -158,7 +165,7 @@ __device__ __forceinline__ uint32_t packed_slice_col128(int kk) { return (kk >> 
 
 // ============================================================== dK / dV
 
-// dK/dV tiles: 128 key rows per CTA (K, V resident), 128-row query blocks
+// dK/dV tiles: 128 key rows per unit (K, V resident), 128-row query blocks
 // streamed, so every MMA runs at full rate (N = 128).  TMEM: S^T (128
 // columns), dP^T (128), dV (D), dK (D): at D = 128 there is no room for a
 // second score buffer, so the compute warps work in two passes per block
@@ -185,6 +192,13 @@ struct DkdvTiles {
   static constexpr uint32_t kTmDK = 256 + D;
 };
 
+// Work units of the dK/dV kernel: (KV block kb, KV head g, batch b), numbered
+// with kb fastest, ascending (under causal masking the first key blocks are
+// seen by the most query blocks: longest first), then g, then b, so that the
+// units in flight at any time share a KV head and re-read the same Q and dO
+// blocks from L2.
+__host__ __device__ __forceinline__ int dkdv_units(const Shape& s) { return ceil_div(s.Tk, 128) * s.HKV * s.B; }
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -192,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const BwdParams p) {
   using C = DkdvTiles<D>;
   constexpr int BQ = 128;  // query rows per streamed block
-  constexpr int BK = 128;  // key rows per CTA
+  constexpr int BK = 128;  // key rows per unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -202,14 +216,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int kb = blockIdx.x;  // small kb sees the most query blocks: launched first
-  const int g = blockIdx.y;
-  const int b = blockIdx.z;
   const int rep = s.H / s.HKV;
-  int qlo, qhi;
-  q_range_for_kv(s.T, s.Tk, BQ, BK, s.causal, s.window, kb, qlo, qhi);
-  const int nqb = qhi - qlo + 1;
-  const int niter = rep * nqb;  // (head r, query block qb) pairs, r outer
+  const int nunits = dkdv_units(s);
+  const int cta = static_cast<int>(blockIdx.x);
+  // unit u -> (kb, g, b) and the query blocks [qlo, qlo + nqb) that see kb;
+  // niter = rep * nqb (head r, query block) pairs, r outer
+  struct Unit {
+    int kb, g, b, qlo, nqb, niter;
+  };
+  auto unit = [&](int u) {
+    Unit w;
+    const int nkb = ceil_div(s.Tk, BK);
+    w.kb = u % nkb;
+    const int r = u / nkb;
+    w.g = r % s.HKV;
+    w.b = r / s.HKV;
+    int qhi;
+    q_range_for_kv(s.T, s.Tk, BQ, BK, s.causal, s.window, w.kb, w.qlo, qhi);
+    w.nqb = qhi - w.qlo + 1;
+    w.niter = rep * w.nqb;
+    return w;
+  };
 
   if (threadIdx.x == 0) init_bars(bars, 1 + 32);
   if (warp == 9) {
@@ -230,60 +257,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
-      if (!p.inject_stall) {
-        mbar_arrive_expect_tx(&bars->res_full, 2 * C::kTile);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, g, kb * BK, b);
-          tma_load_4d(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, g, kb * BK, b);
-        }
-      }
     }
-    // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
-    // four per lane; read one block ahead so that their latency overlaps the
-    // wait for the stage
-    float l2[4], dl[4];
-    auto load_rows = [&](int n) {
-      const int h = g * rep + n / nqb;
-      const int qb = qlo + n % nqb;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = qb * BQ + lane + 32 * k;
-        l2[k] = 0.f;
-        dl[k] = 0.f;
-        if (i < s.T) {
-          const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
-          l2[k] = -p.LSE[idx] * kLog2e;
-          dl[k] = p.Delta[idx];
-        }
-      }
-    };
-    if (niter > 0) load_rows(0);
-    int issued = 0;
-    for (int n = 0; n < niter; ++n) {
-      const int st = n % C::kStages;
-      if (n >= C::kStages && !warp_wait(&bars->x_empty[st], ((n / C::kStages) - 1) & 1, ctl, kCode)) break;
-      const int h = g * rep + n / nqb;
-      const int qb = qlo + n % nqb;
-      mbar_arrive_expect_tx_e(&bars->x_full[st], 2 * C::kTile);  // one elected lane arms and copies
+    int xc = 0, uc = 0;  // streamed stages and units issued by this CTA
+    bool ok = true;
+    int u = cta;  // the CTA's first unit; later ones are claimed from the counter
+    for (int seq = 0; ok && !p.inject_stall; ++seq) {
+      if (!(ok = sched_publish(&bars->sched, seq, u, ctl, kCode))) break;
+      if (u >= nunits) break;  // the end marker has been handed on
+      const Unit w = unit(u);
+      // K and V of this unit once the previous unit's MMAs are done with them
+      if (uc > 0 && !(ok = warp_wait(&bars->res_empty, (uc - 1) & 1, ctl, kCode))) break;
+      mbar_arrive_expect_tx_e(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d_e(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
-                      qb * BQ, b);
-        tma_load_4d_e(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
-                      qb * BQ, b);
+        tma_load_4d_e(&tmK, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, w.g, w.kb * BK, w.b);
+        tma_load_4d_e(&tmV, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, w.g, w.kb * BK, w.b);
       }
-      float* rows = srows + st * 256;
+      ++uc;
+      // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
+      // four per lane; read one block ahead so that their latency overlaps the
+      // wait for the stage
+      float l2[4], dl[4];
+      auto load_rows = [&](int n) {
+        const int h = w.g * rep + n / w.nqb;
+        const int qb = w.qlo + n % w.nqb;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        rows[lane + 32 * k] = l2[k];
-        rows[128 + lane + 32 * k] = dl[k];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int i = qb * BQ + lane + 32 * q4;
+          l2[q4] = 0.f;
+          dl[q4] = 0.f;
+          if (i < s.T) {
+            const size_t idx = (static_cast<size_t>(w.b) * s.H + h) * s.T + i;
+            l2[q4] = -p.LSE[idx] * kLog2e;
+            dl[q4] = p.Delta[idx];
+          }
+        }
+      };
+      if (w.niter > 0) load_rows(0);
+      for (int n = 0; n < w.niter; ++n) {
+        const int st = xc % C::kStages;
+        if (xc >= C::kStages && !(ok = warp_wait(&bars->x_empty[st], ((xc / C::kStages) - 1) & 1, ctl, kCode)))
+          break;
+        const int h = w.g * rep + n / w.nqb;
+        const int qb = w.qlo + n % w.nqb;
+        mbar_arrive_expect_tx_e(&bars->x_full[st], 2 * C::kTile);  // one elected lane arms and copies
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d_e(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
+                        qb * BQ, w.b);
+          tma_load_4d_e(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
+                        qb * BQ, w.b);
+        }
+        float* rows = srows + st * 256;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          rows[lane + 32 * q4] = l2[q4];
+          rows[128 + lane + 32 * q4] = dl[q4];
+        }
+        mbar_arrive(&bars->x_full[st]);
+        ++xc;
+        if (n + 1 < w.niter) load_rows(n + 1);
       }
-      mbar_arrive(&bars->x_full[st]);
-      issued = n + 1;
-      if (n + 1 < niter) load_rows(n + 1);
+      // claim the next unit only now, near the end of this one, so that the
+      // CTAs that finish first take the next longest units
+      int claimed = 0;
+      if (lane == 0) claimed = sched_claim(p.sched);
+      u = __shfl_sync(0xffffffffu, claimed, 0);
     }
     if (lane == 0 && bars->abort) {
-      if (!p.inject_stall) drain_bar(&bars->res_full, 0, p.timeout_ns);
-      for (int n = imax(0, issued - C::kStages); n < issued; ++n)
+      if (uc > 0) drain_bar(&bars->res_full, (uc - 1) & 1, p.timeout_ns);
+      for (int n = imax(0, xc - C::kStages); n < xc; ++n)
         drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
@@ -293,16 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sK = sbase + C::kOffRes0;
       const uint32_t sV = sbase + C::kOffRes1;
-      auto issue_s = [&](int n) -> bool {  // S^T_n = K Q_n^T
-        const int st = n % C::kStages;
-        if (!warp_wait(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode)) return false;
+      int xc = 0, uc = 0;  // streamed stages and units consumed (x_full, p/ds phases run with xc)
+      auto issue_s = [&](int xg) -> bool {  // S^T = K Q^T of streamed stage xg
+        const int st = xg % C::kStages;
+        if (!warp_wait(&bars->x_full[st], (xg / C::kStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
         issue_kk<D>(tmem + C::kTmS, sK, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk, idesc_s);
         mma_commit_e(&bars->s_full[0]);
         return true;
       };
-      auto issue_dp = [&](int n) {  // dP^T_n = V dO_n^T (stage already waited for by issue_s)
-        issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + (n % C::kStages) * C::kTile, C::kChunk,
+      auto issue_dp = [&](int xg) {  // dP^T = V dO^T (stage already waited for by issue_s)
+        issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + (xg % C::kStages) * C::kTile, C::kChunk,
                     idesc_s);
         mma_commit_e(&bars->dp_full[0]);
       };
@@ -312,26 +354,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk)
           mma_ts_e(acc, a_tmem + packed_slice_col128(kk), b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc,
-                 (accumulate || kk > 0) ? 1u : 0u);
+                   (accumulate || kk > 0) ? 1u : 0u);
       };
-      bool ok = warp_wait(&bars->res_full, 0, ctl, kCode);
-      if (ok && niter > 0) {
-        ok = issue_s(0);
-        if (ok) issue_dp(0);
-      }
-      for (int n = 0; ok && n < niter; ++n) {
-        const int st = n % C::kStages;
-        if (!(ok = warp_wait(&bars->p_full[0], n & 1, ctl, kCode))) break;
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int u = sched_next(&bars->sched, seq, ctl, kCode);
+        if (u < 0) {
+          ok = false;
+          break;
+        }
+        if (u >= nunits) break;
+        const Unit w = unit(u);
+        if (!(ok = warp_wait(&bars->res_full, uc & 1, ctl, kCode))) break;
         tc_fence_after();
-        issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + st * C::kTile, n > 0);  // dV += P^T dO
-        if (n + 1 < niter && !(ok = issue_s(n + 1))) break;  // P^T_n is read by the dV MMAs queued above
-        if (!(ok = warp_wait(&bars->ds_full[0], n & 1, ctl, kCode))) break;
-        tc_fence_after();
-        issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + st * C::kTile, n > 0);  // dK += dS^T Q
-        mma_commit_e(&bars->x_empty[st]);
-        if (n + 1 < niter) issue_dp(n + 1);  // dS^T_n is read by the dK MMAs queued above
+        ++uc;
+        if (w.niter > 0) {
+          if (!(ok = issue_s(xc))) break;
+          issue_dp(xc);
+        }
+        if (w.niter <= 1) mma_commit_e(&bars->res_empty);  // every MMA reading K and V is issued
+        for (int n = 0; ok && n < w.niter; ++n) {
+          const int xg = xc + n;
+          const int st = xg % C::kStages;
+          if (!(ok = warp_wait(&bars->p_full[0], xg & 1, ctl, kCode))) break;
+          tc_fence_after();
+          issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + st * C::kTile, n > 0);  // dV += P^T dO
+          if (n + 1 < w.niter && !(ok = issue_s(xg + 1))) break;  // P^T_n is read by the dV MMAs queued above
+          if (!(ok = warp_wait(&bars->ds_full[0], xg & 1, ctl, kCode))) break;
+          tc_fence_after();
+          issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + st * C::kTile, n > 0);  // dK += dS^T Q
+          mma_commit_e(&bars->x_empty[st]);
+          if (n + 1 < w.niter) {
+            issue_dp(xg + 1);  // dS^T_n is read by the dK MMAs queued above
+            if (n + 2 == w.niter) mma_commit_e(&bars->res_empty);  // the unit's last MMAs reading K and V
+          }
+        }
+        if (!ok) break;
+        mma_commit_e(&bars->acc_full);
+        xc += w.niter;
       }
-      if (ok) mma_commit_e(&bars->acc_full);
       mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
@@ -340,104 +401,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;          // TMEM lane quarter
     const int half = warp >> 2;            // 64-column half of each 128-column tile
     const int jrow = quarter * 32 + lane;  // key row within the block (TMEM lane)
-    const int j = kb * BK + jrow;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + C::kTmS + half * 64;
     const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
     const float sl2 = p.scale_log2;
+    int xc = 0, uc = 0;
     bool ok = true;
-    for (int n = 0; ok && n < niter; ++n) {
-      const int st = n % C::kStages;
-      const int qb = qlo + n % nqb;
-      const float* rows = srows + st * 256 + half * 64;
-      // pass 1: P^T = 2^(S^T*scale*log2e - LSE*log2e), masked -> bf16 over S^T
-      if (!(ok = warp_wait(&bars->s_full[0], n & 1, ctl, kCode))) break;
-      if (!(ok = warp_wait(&bars->x_full[st], (n / C::kStages) & 1, ctl, kCode))) break;  // rows visible
-      tc_fence_after();
-      const bool need_mask = block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb);
-      float pv[64];
-      {
-        float lo[32], hi[32];
-        load_two_cols32(s_addr, s_addr + 32, lo, hi);
+    for (int seq = 0; ok; ++seq) {
+      const int u = sched_next(&bars->sched, seq, ctl, kCode);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= nunits) break;
+      const Unit w = unit(u);
+      const int j = w.kb * BK + jrow;
+      for (int n = 0; ok && n < w.niter; ++n) {
+        const int xg = xc + n;
+        const int st = xg % C::kStages;
+        const int qb = w.qlo + n % w.nqb;
+        const float* rows = srows + st * 256 + half * 64;
+        // pass 1: P^T = 2^(S^T*scale*log2e - LSE*log2e), masked -> bf16 over S^T
+        if (!(ok = warp_wait(&bars->s_full[0], xg & 1, ctl, kCode))) break;
+        if (!(ok = warp_wait(&bars->x_full[st], (xg / C::kStages) & 1, ctl, kCode))) break;  // rows visible
+        tc_fence_after();
+        const bool need_mask = block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, w.kb);
+        float pv[64];
+        {
+          float lo[32], hi[32];
+          load_two_cols32(s_addr, s_addr + 32, lo, hi);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          pv[c] = lo[c];
-          pv[32 + c] = hi[c];
+          for (int c = 0; c < 32; ++c) {
+            pv[c] = lo[c];
+            pv[32 + c] = hi[c];
+          }
         }
-      }
-      const float4* lse4 = reinterpret_cast<const float4*>(rows);  // -LSE*log2e per query
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const float4* lse4 = reinterpret_cast<const float4*>(rows);  // -LSE*log2e per query
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l = lse4[c4];
-        float x0, x1, x2, x3;
-        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]), sl2x2, f2_pack(l.x, l.y)), x0, x1);
-        f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2, f2_pack(l.z, l.w)), x2, x3);
-        pv[4 * c4 + 0] = ex2(x0);
-        pv[4 * c4 + 1] = ex2(x1);
-        pv[4 * c4 + 2] = ex2(x2);
-        pv[4 * c4 + 3] = ex2(x3);
-      }
-      if (need_mask) {
-        // the visibility rule element by element (the [lo, hi] range form
-        // the other kernels use measured 3 % slower here on the long causal
-        // workload: it changed this kernel's register allocation)
-        const int i0 = qb * BQ + half * 64;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const int i = i0 + c;
-          const bool hide = i >= s.T || j >= s.Tk || (s.causal && j > i) || (s.window > 0 && i - j >= s.window);
-          pv[c] = hide ? 0.f : pv[c];
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l = lse4[c4];
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]), sl2x2, f2_pack(l.x, l.y)), x0, x1);
+          f2_unpack(f2_fma(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]), sl2x2, f2_pack(l.z, l.w)), x2, x3);
+          pv[4 * c4 + 0] = ex2(x0);
+          pv[4 * c4 + 1] = ex2(x1);
+          pv[4 * c4 + 2] = ex2(x2);
+          pv[4 * c4 + 3] = ex2(x3);
         }
-      }
-      {
+        if (need_mask) {
+          // the visibility rule element by element (the [lo, hi] range form
+          // the other kernels use measured 3 % slower here on the long causal
+          // workload: it changed this kernel's register allocation)
+          const int i0 = qb * BQ + half * 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int i = i0 + c;
+            const bool hide = i >= s.T || j >= s.Tk || (s.causal && j > i) || (s.window > 0 && i - j >= s.window);
+            pv[c] = hide ? 0.f : pv[c];
+          }
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pk[e] = pack2<F16>(pv[2 * e], pv[2 * e + 1]);
+          tmem_st32(s_addr, pk);  // 64 packed values into the first 32 columns of this half
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&bars->p_full[0]);
+        // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T
+        if (!(ok = warp_wait(&bars->dp_full[0], xg & 1, ctl, kCode))) break;
+        tc_fence_after();
+        float dlo[32], dhi[32];
+        load_two_cols32(dp_addr, dp_addr + 32, dlo, dhi);
+        const float4* del4 = reinterpret_cast<const float4*>(rows + 128);
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack2<F16>(pv[2 * e], pv[2 * e + 1]);
-        tmem_st32(s_addr, pk);  // 64 packed values into the first 32 columns of this half
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&bars->p_full[0]);
-      // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T
-      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
-      tc_fence_after();
-      float dlo[32], dhi[32];
-      load_two_cols32(dp_addr, dp_addr + 32, dlo, dhi);
-      const float4* del4 = reinterpret_cast<const float4*>(rows + 128);
-      uint32_t pk[32];
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d = del4[c4];
+          const float4 e = del4[8 + c4];
+          // dS = P (dP - Delta), paired
+          f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]),
+                           f2_sub(f2_pack(dlo[4 * c4 + 0], dlo[4 * c4 + 1]), f2_pack(d.x, d.y))),
+                    dlo[4 * c4 + 0], dlo[4 * c4 + 1]);
+          f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
+                           f2_sub(f2_pack(dlo[4 * c4 + 2], dlo[4 * c4 + 3]), f2_pack(d.z, d.w))),
+                    dlo[4 * c4 + 2], dlo[4 * c4 + 3]);
+          f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 0], pv[32 + 4 * c4 + 1]),
+                           f2_sub(f2_pack(dhi[4 * c4 + 0], dhi[4 * c4 + 1]), f2_pack(e.x, e.y))),
+                    dhi[4 * c4 + 0], dhi[4 * c4 + 1]);
+          f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 2], pv[32 + 4 * c4 + 3]),
+                           f2_sub(f2_pack(dhi[4 * c4 + 2], dhi[4 * c4 + 3]), f2_pack(e.z, e.w))),
+                    dhi[4 * c4 + 2], dhi[4 * c4 + 3]);
+        }
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 d = del4[c4];
-        const float4 e = del4[8 + c4];
-        // dS = P (dP - Delta), paired
-        f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 0], pv[4 * c4 + 1]),
-                         f2_sub(f2_pack(dlo[4 * c4 + 0], dlo[4 * c4 + 1]), f2_pack(d.x, d.y))),
-                  dlo[4 * c4 + 0], dlo[4 * c4 + 1]);
-        f2_unpack(f2_mul(f2_pack(pv[4 * c4 + 2], pv[4 * c4 + 3]),
-                         f2_sub(f2_pack(dlo[4 * c4 + 2], dlo[4 * c4 + 3]), f2_pack(d.z, d.w))),
-                  dlo[4 * c4 + 2], dlo[4 * c4 + 3]);
-        f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 0], pv[32 + 4 * c4 + 1]),
-                         f2_sub(f2_pack(dhi[4 * c4 + 0], dhi[4 * c4 + 1]), f2_pack(e.x, e.y))),
-                  dhi[4 * c4 + 0], dhi[4 * c4 + 1]);
-        f2_unpack(f2_mul(f2_pack(pv[32 + 4 * c4 + 2], pv[32 + 4 * c4 + 3]),
-                         f2_sub(f2_pack(dhi[4 * c4 + 2], dhi[4 * c4 + 3]), f2_pack(e.z, e.w))),
-                  dhi[4 * c4 + 2], dhi[4 * c4 + 3]);
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack2<F16>(dlo[2 * e], dlo[2 * e + 1]);
+          pk[16 + e] = pack2<F16>(dhi[2 * e], dhi[2 * e + 1]);
+        }
+        tmem_st32(dp_addr, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&bars->ds_full[0]);
       }
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        pk[e] = pack2<F16>(dlo[2 * e], dlo[2 * e + 1]);
-        pk[16 + e] = pack2<F16>(dhi[2 * e], dhi[2 * e + 1]);
-      }
-      tmem_st32(dp_addr, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&bars->ds_full[0]);
-    }
-    if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
-    if (ok) {
+      if (!ok) break;
+      xc += w.niter;
+      if (!(ok = warp_wait(&bars->acc_full, uc & 1, ctl, kCode))) break;
+      ++uc;
       tc_fence_after();
-      const size_t rowoff = ((static_cast<size_t>(b) * s.Tk + j) * s.HKV + g) * s.D + half * (D / 2);
+      const size_t rowoff = ((static_cast<size_t>(w.b) * s.Tk + j) * s.HKV + w.g) * s.D + half * (D / 2);
       const int nvalid = s.D - half * (D / 2);  // columns of this half inside the head dim
       store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, nvalid, 1.f,
                          static_cast<uint16_t*>(p.dV) + rowoff, j < s.Tk);
@@ -448,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) sched_exit(p.sched);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
@@ -482,13 +556,18 @@ struct DqTiles {
   static constexpr uint32_t kTmDQ = 384;  // D columns
 };
 
+// Work units of the dQ kernel: (query block qb, head h, batch b), numbered
+// with qb fastest from the end of the sequence (longest causal work first),
+// then h, then b, so that the units in flight at any time share a KV head.
+__host__ __device__ __forceinline__ int dq_units(const Shape& s) { return ceil_div(s.T, 128) * s.H * s.B; }
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                           const BwdParams p) {
   using C = DqTiles<D>;
-  constexpr int BQ = 128;  // query rows per CTA
+  constexpr int BQ = 128;  // query rows per unit
   constexpr int BK = 128;  // key rows per streamed block
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -499,13 +578,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nq = ceil_div(s.T, BQ);
-  const int qb = nq - 1 - static_cast<int>(blockIdx.x);  // longest causal tiles first
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int g = h / (s.H / s.HKV);
-  int kb_lo, kb_hi;
-  kv_range_for_q(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb_lo, kb_hi);
-  const int nblk = kb_hi - kb_lo + 1;
+  const int nunits = dq_units(s);
+  const int cta = static_cast<int>(blockIdx.x);
+  // unit u -> (qb, h, b, g) and the visible KV blocks [kb_lo, kb_lo + nblk)
+  struct Unit {
+    int qb, h, b, g, kb_lo, nblk;
+  };
+  auto unit = [&](int u) {
+    Unit w;
+    const int x = u % nq;
+    const int r = u / nq;
+    w.qb = nq - 1 - x;
+    w.h = r % s.H;
+    w.b = r / s.H;
+    w.g = w.h / (s.H / s.HKV);
+    int kb_hi;
+    kv_range_for_q(s.T, s.Tk, BQ, BK, s.causal, s.window, w.qb, w.kb_lo, kb_hi);
+    w.nblk = kb_hi - w.kb_lo + 1;
+    return w;
+  };
 
   if (threadIdx.x == 0) init_bars(bars, 1);
   if (warp == 9) {
@@ -529,35 +620,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmV);
       prefetch_tmap(&tmdO);
     }
-    if (!p.inject_stall) {
+    int kc = 0, vc = 0, uc = 0;  // K blocks, V blocks and units issued by this CTA
+    bool ok = true;
+    int u = cta;  // the CTA's first unit; later ones are claimed from the counter
+    for (int seq = 0; ok && !p.inject_stall; ++seq) {
+      if (!(ok = sched_publish(&bars->sched, seq, u, ctl, kCode))) break;
+      if (u >= nunits) break;  // the end marker has been handed on
+      const Unit w = unit(u);
+      // Q and dO of this unit once the previous unit's MMAs are done with them
+      if (uc > 0 && !(ok = warp_wait(&bars->res_empty, (uc - 1) & 1, ctl, kCode))) break;
       mbar_arrive_expect_tx_e(&bars->res_full, 2 * C::kTile);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d_e(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, h, qb * BQ, b);
-        tma_load_4d_e(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, h, qb * BQ, b);
+        tma_load_4d_e(&tmQ, &bars->res_full, smem + C::kOffRes0 + c * C::kChunk, c * 64, w.h, w.qb * BQ, w.b);
+        tma_load_4d_e(&tmdO, &bars->res_full, smem + C::kOffRes1 + c * C::kChunk, c * 64, w.h, w.qb * BQ, w.b);
       }
-    }
-    int issued_k = 0, issued_v = 0;
-    for (int n = 0; n < nblk; ++n) {
-      const int sk = n % C::kKStages;
-      if (n >= C::kKStages && !warp_wait(&bars->x_empty[sk], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
-      mbar_arrive_expect_tx_e(&bars->x_full[sk], C::kTile);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d_e(&tmK, &bars->x_full[sk], smem + C::kOffK + sk * C::kTile + c * C::kChunk, c * 64, g,
-                      (kb_lo + n) * BK, b);
-      issued_k = n + 1;
-      const int sv = n % C::kVStages;
-      if (n >= C::kVStages && !warp_wait(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
-      mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTile);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTile + c * C::kChunk, c * 64, g,
-                      (kb_lo + n) * BK, b);
-      issued_v = n + 1;
+      ++uc;
+      for (int n = 0; n < w.nblk; ++n) {
+        const int sk = kc % C::kKStages;
+        if (kc >= C::kKStages && !(ok = warp_wait(&bars->x_empty[sk], ((kc / C::kKStages) - 1) & 1, ctl, kCode)))
+          break;
+        mbar_arrive_expect_tx_e(&bars->x_full[sk], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d_e(&tmK, &bars->x_full[sk], smem + C::kOffK + sk * C::kTile + c * C::kChunk, c * 64, w.g,
+                        (w.kb_lo + n) * BK, w.b);
+        ++kc;
+        const int sv = vc % C::kVStages;
+        if (vc >= C::kVStages && !(ok = warp_wait(&bars->v_empty[sv], ((vc / C::kVStages) - 1) & 1, ctl, kCode)))
+          break;
+        mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTile + c * C::kChunk, c * 64, w.g,
+                        (w.kb_lo + n) * BK, w.b);
+        ++vc;
+      }
+      // claim the next unit only now, near the end of this one, so that the
+      // CTAs that finish first take the next longest units
+      int claimed = 0;
+      if (lane == 0) claimed = sched_claim(p.sched);
+      u = __shfl_sync(0xffffffffu, claimed, 0);
     }
     if (bars->abort) {
-      if (!p.inject_stall) drain_bar(&bars->res_full, 0, p.timeout_ns);
-      for (int n = imax(0, issued_k - C::kKStages); n < issued_k; ++n)
+      if (uc > 0) drain_bar(&bars->res_full, (uc - 1) & 1, p.timeout_ns);
+      for (int n = imax(0, kc - C::kKStages); n < kc; ++n)
         drain_bar(&bars->x_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
-      for (int n = imax(0, issued_v - C::kVStages); n < issued_v; ++n)
+      for (int n = imax(0, vc - C::kVStages); n < vc; ++n)
         drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
@@ -566,45 +672,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_acc = idesc_f32acc<F16>(128, D, false, true);  // TMEM A x MN-major B, N = D
       const uint32_t sQ = sbase + C::kOffRes0;
       const uint32_t sdO = sbase + C::kOffRes1;
-      auto issue_s = [&](int n) -> bool {  // S_n = Q K_n^T into buffer n & 1
-        const int st = n % C::kKStages;
-        if (!warp_wait(&bars->x_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
+      // streamed blocks consumed by this CTA: block bg uses K stage
+      // bg % kKStages, V stage bg % kVStages and S buffer bg & 1
+      auto issue_s = [&](int bg) -> bool {  // S = Q K^T into buffer bg & 1
+        const int st = bg % C::kKStages;
+        if (!warp_wait(&bars->x_full[st], (bg / C::kKStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
-        issue_kk<D>(tmem + C::kTmS + (n & 1) * 128, sQ, C::kChunk, sbase + C::kOffK + st * C::kTile, C::kChunk,
+        issue_kk<D>(tmem + C::kTmS + (bg & 1) * 128, sQ, C::kChunk, sbase + C::kOffK + st * C::kTile, C::kChunk,
                     idesc_s);
-        mma_commit_e(&bars->s_full[n & 1]);
+        mma_commit_e(&bars->s_full[bg & 1]);
         return true;
       };
-      auto issue_dp = [&](int n) -> bool {  // dP_n = dO V_n^T; its V stage is free once this completes
-        const int st = n % C::kVStages;
-        if (!warp_wait(&bars->v_full[st], (n / C::kVStages) & 1, ctl, kCode)) return false;
+      auto issue_dp = [&](int bg) -> bool {  // dP = dO V^T; its V stage is free once this completes
+        const int st = bg % C::kVStages;
+        if (!warp_wait(&bars->v_full[st], (bg / C::kVStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
         issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffV + st * C::kTile, C::kChunk, idesc_s);
         mma_commit_e(&bars->dp_full[0]);
         mma_commit_e(&bars->v_empty[st]);
         return true;
       };
-      bool ok = warp_wait(&bars->res_full, 0, ctl, kCode);
-      if (ok && nblk > 0) {
-        ok = issue_s(0);
-        if (ok) ok = issue_dp(0);
-      }
-      // queue order: S0 dP0 S1 | dP1 dQ0 S2 | dP2 dQ1 S3 ...
-      for (int n = 0; ok && n < nblk; ++n) {
-        if (n + 1 < nblk && !(ok = issue_s(n + 1))) break;
-        const int st = n % C::kKStages;
-        if (!(ok = warp_wait(&bars->ds_full[0], n & 1, ctl, kCode))) break;
+      int bc = 0, uc = 0;
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int u = sched_next(&bars->sched, seq, ctl, kCode);
+        if (u < 0) {
+          ok = false;
+          break;
+        }
+        if (u >= nunits) break;
+        const Unit w = unit(u);
+        if (!(ok = warp_wait(&bars->res_full, uc & 1, ctl, kCode))) break;
         tc_fence_after();
-        if (n + 1 < nblk && !(ok = issue_dp(n + 1))) break;  // dP_n has been read: its columns are free
-        // dQ += dS K   (K = the block's 128 key rows)
-        const uint64_t b0 = sdesc_sw128(sbase + C::kOffK + st * C::kTile, C::kChunk, 1024);
+        ++uc;
+        if (w.nblk > 0) {
+          if (!(ok = issue_s(bc))) break;
+          if (!(ok = issue_dp(bc))) break;
+        }
+        if (w.nblk <= 1) mma_commit_e(&bars->res_empty);  // every MMA reading Q and dO is issued
+        // queue order: S0 dP0 S1 | dP1 dQ0 S2 | dP2 dQ1 S3 ...
+        for (int n = 0; ok && n < w.nblk; ++n) {
+          const int bg = bc + n;
+          if (n + 1 < w.nblk && !(ok = issue_s(bg + 1))) break;
+          const int st = bg % C::kKStages;
+          if (!(ok = warp_wait(&bars->ds_full[0], bg & 1, ctl, kCode))) break;
+          tc_fence_after();
+          if (n + 1 < w.nblk) {
+            if (!(ok = issue_dp(bg + 1))) break;  // dP_n has been read: its columns are free
+            if (n + 2 == w.nblk) mma_commit_e(&bars->res_empty);  // the unit's last MMAs reading Q and dO
+          }
+          // dQ += dS K   (K = the block's 128 key rows)
+          const uint64_t b0 = sdesc_sw128(sbase + C::kOffK + st * C::kTile, C::kChunk, 1024);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_ts_e(tmem + C::kTmDQ, tmem + C::kTmS + (n & 1) * 128 + packed_slice_col128(kk),
-                 b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_e(&bars->x_empty[st]);
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ts_e(tmem + C::kTmDQ, tmem + C::kTmS + (bg & 1) * 128 + packed_slice_col128(kk),
+                     b0 + ((kk * 16 * kRowBytes) >> 4), idesc_acc, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_e(&bars->x_empty[st]);
+        }
+        if (!ok) break;
+        mma_commit_e(&bars->acc_full);
+        bc += w.nblk;
       }
-      if (ok) mma_commit_e(&bars->acc_full);
       mma_commit_e(&bars->drain);
       drain_bar(&bars->drain, 0, p.timeout_ns);
     }
@@ -612,75 +740,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int half = warp >> 2;  // 64-key half of each 128-key block
     const int irow = quarter * 32 + lane;
-    const int i = qb * BQ + irow;
-    int vis_lo, vis_hi;  // keys row i sees
-    visible_keys(s.T, s.Tk, s.causal, s.window, i, vis_lo, vis_hi);
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    float lse2 = 0.f, delta = 0.f;
-    if (i < s.T) {
-      const size_t idx = (static_cast<size_t>(b) * s.H + h) * s.T + i;
-      lse2 = p.LSE[idx] * kLog2e;
-      delta = p.Delta[idx];
-    }
+    int bc = 0, uc = 0;
     bool ok = true;
-    for (int n = 0; ok && n < nblk; ++n) {
-      const int kb = kb_lo + n;
-      const int bf = n & 1;
-      // pass 1 (overlaps the dP MMA of this block): P = 2^(S*scale*log2e - LSE*log2e), masked
-      if (!(ok = warp_wait(&bars->s_full[bf], (n >> 1) & 1, ctl, kCode))) break;
-      tc_fence_after();
-      const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 128 + half * 64;
-      const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
-      float pv[64];
-      {
-        float lo[32], hi[32];
-        load_two_cols32(s_addr, s_addr + 32, lo, hi);
-        const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
+    for (int seq = 0; ok; ++seq) {
+      const int u = sched_next(&bars->sched, seq, ctl, kCode);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= nunits) break;
+      const Unit w = unit(u);
+      const int i = w.qb * BQ + irow;
+      int vis_lo, vis_hi;  // keys row i sees
+      visible_keys(s.T, s.Tk, s.causal, s.window, i, vis_lo, vis_hi);
+      float lse2 = 0.f, delta = 0.f;
+      if (i < s.T) {
+        const size_t idx = (static_cast<size_t>(w.b) * s.H + w.h) * s.T + i;
+        lse2 = p.LSE[idx] * kLog2e;
+        delta = p.Delta[idx];
+      }
+      for (int n = 0; ok && n < w.nblk; ++n) {
+        const int kb = w.kb_lo + n;
+        const int bg = bc + n;
+        const int bf = bg & 1;
+        // pass 1 (overlaps the dP MMA of this block): P = 2^(S*scale*log2e - LSE*log2e), masked
+        if (!(ok = warp_wait(&bars->s_full[bf], (bg >> 1) & 1, ctl, kCode))) break;
+        tc_fence_after();
+        const uint32_t s_addr = tmem + lane_addr + C::kTmS + bf * 128 + half * 64;
+        const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
+        float pv[64];
+        {
+          float lo[32], hi[32];
+          load_two_cols32(s_addr, s_addr + 32, lo, hi);
+          const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float x0, x1, y0, y1;
-          f2_unpack(f2_fma(f2_pack(lo[c], lo[c + 1]), sl2x2, nl2), x0, x1);
-          f2_unpack(f2_fma(f2_pack(hi[c], hi[c + 1]), sl2x2, nl2), y0, y1);
-          pv[c] = ex2(x0);
-          pv[c + 1] = ex2(x1);
-          pv[32 + c] = ex2(y0);
-          pv[33 + c] = ex2(y1);
+          for (int c = 0; c < 32; c += 2) {
+            float x0, x1, y0, y1;
+            f2_unpack(f2_fma(f2_pack(lo[c], lo[c + 1]), sl2x2, nl2), x0, x1);
+            f2_unpack(f2_fma(f2_pack(hi[c], hi[c + 1]), sl2x2, nl2), y0, y1);
+            pv[c] = ex2(x0);
+            pv[c + 1] = ex2(x1);
+            pv[32 + c] = ex2(y0);
+            pv[33 + c] = ex2(y1);
+          }
         }
-      }
-      if (block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb)) {
-        // the keys this row sees, relative to the 64 columns
-        const int a = vis_lo - (kb * BK + half * 64), z = vis_hi - (kb * BK + half * 64);
+        if (block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, w.qb, kb)) {
+          // the keys this row sees, relative to the 64 columns
+          const int a = vis_lo - (kb * BK + half * 64), z = vis_hi - (kb * BK + half * 64);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pv[c] = (c < a || c > z) ? 0.f : pv[c];
-      }
-      // pass 2: dS = P (dP - Delta) -> bf16 over the S columns this thread read
-      if (!(ok = warp_wait(&bars->dp_full[0], n & 1, ctl, kCode))) break;
-      tc_fence_after();
-      {
-        float lo[32], hi[32];
-        load_two_cols32(dp_addr, dp_addr + 32, lo, hi);
-        uint32_t pk[32];
-        const uint64_t dl2 = f2_pack(delta, delta);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {  // dS = P (dP - Delta), paired
-          float a0, a1, b0, b1;
-          f2_unpack(f2_mul(f2_pack(pv[2 * e], pv[2 * e + 1]), f2_sub(f2_pack(lo[2 * e], lo[2 * e + 1]), dl2)), a0, a1);
-          f2_unpack(f2_mul(f2_pack(pv[32 + 2 * e], pv[33 + 2 * e]), f2_sub(f2_pack(hi[2 * e], hi[2 * e + 1]), dl2)), b0,
-                    b1);
-          pk[e] = pack2<F16>(a0, a1);
-          pk[16 + e] = pack2<F16>(b0, b1);
+          for (int c = 0; c < 64; ++c) pv[c] = (c < a || c > z) ? 0.f : pv[c];
         }
-        tmem_st32(s_addr, pk);  // dS of keys [64 half, 64 half + 64) -> columns [64 half, 64 half + 32)
+        // pass 2: dS = P (dP - Delta) -> bf16 over the S columns this thread read
+        if (!(ok = warp_wait(&bars->dp_full[0], bg & 1, ctl, kCode))) break;
+        tc_fence_after();
+        {
+          float lo[32], hi[32];
+          load_two_cols32(dp_addr, dp_addr + 32, lo, hi);
+          uint32_t pk[32];
+          const uint64_t dl2 = f2_pack(delta, delta);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {  // dS = P (dP - Delta), paired
+            float a0, a1, b0, b1;
+            f2_unpack(f2_mul(f2_pack(pv[2 * e], pv[2 * e + 1]), f2_sub(f2_pack(lo[2 * e], lo[2 * e + 1]), dl2)), a0,
+                      a1);
+            f2_unpack(f2_mul(f2_pack(pv[32 + 2 * e], pv[33 + 2 * e]), f2_sub(f2_pack(hi[2 * e], hi[2 * e + 1]), dl2)),
+                      b0, b1);
+            pk[e] = pack2<F16>(a0, a1);
+            pk[16 + e] = pack2<F16>(b0, b1);
+          }
+          tmem_st32(s_addr, pk);  // dS of keys [64 half, 64 half + 64) -> columns [64 half, 64 half + 32)
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&bars->ds_full[0]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&bars->ds_full[0]);
-    }
-    if (ok) ok = warp_wait(&bars->acc_full, 0, ctl, kCode);
-    if (ok) {
+      if (!ok) break;
+      bc += w.nblk;
+      if (!(ok = warp_wait(&bars->acc_full, uc & 1, ctl, kCode))) break;
+      ++uc;
       tc_fence_after();
-      const size_t rowoff = ((static_cast<size_t>(b) * s.T + i) * s.H + h) * s.D + half * (D / 2);
+      const size_t rowoff = ((static_cast<size_t>(w.b) * s.T + i) * s.H + w.h) * s.D + half * (D / 2);
       store_acc_row<F16>(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.D - half * (D / 2), s.scale,
                          static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T);
     }
@@ -688,6 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) sched_exit(p.sched);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
@@ -705,7 +847,7 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(p.s.Tk, 128), p.s.HKV, p.s.B);
+  const dim3 grid(imax(1, imin(p.ctas, dkdv_units(p.s))));
   fa_bwd_dkdv_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }
@@ -720,7 +862,7 @@ cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t s
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(p.s.T, 128), p.s.H, p.s.B);
+  const dim3 grid(imax(1, imin(p.ctas, dq_units(p.s))));
   fa_bwd_dq_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
 }

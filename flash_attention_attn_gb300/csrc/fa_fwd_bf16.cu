@@ -30,6 +30,7 @@
 #include <math_constants.h>
 
 #include "fa_internal.h"
+#include "fa_sched.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -358,18 +359,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- two tiles
 //
-// Two 128-row query tiles A and B per CTA, sharing every K/V block the CTA
-// streams: one query block of two query heads that share a KV head (head
-// pairs, when H/HKV is even; both tiles see the same key range) or query
-// blocks 2j and 2j + 1 of one head (block pairs).  Each 64 KB K/V block
+// Two 128-row query tiles A and B per work unit, sharing every K/V block the
+// unit streams: one query block of two query heads that share a KV head
+// (head pairs, when H/HKV is even; both tiles see the same key range) or
+// query blocks 2j and 2j + 1 of one head (block pairs).  Each 64 KB K/V block
 // (D = 128) feeds four 128x128 MMA groups instead of two, which halves the
 // TMA traffic per MMA.  Measured on GB300, a K/V ring feeding one tile is
 // bounded near 1600 cycles per block by the TMA stream itself against 1024
 // cycles of MMAs.
+//
+// Persistent: at most one CTA per SM, each walking its share of the units
+// (longest causal work first, snake order across CTAs).  Barriers, TMEM and
+// the K/V rings live for the whole launch and their phases run on across
+// units, so the next unit's Q and first K/V blocks load while the current
+// unit finishes, and its first score MMAs run while the softmax warps store
+// the current unit's O.
 //   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B (warp w owns
 //             TMEM lanes 32*(w%4).. = rows of its tile)
-//   warp  8   TMA producer: Q_A, Q_B, then K and V blocks in the order the
-//             MMAs need them
+//   warp  8   TMA producer: per unit Q_A, Q_B (once the previous unit's
+//             score MMAs are done with them), then K and V blocks in the
+//             order the MMAs need them
 //   warp  9   MMA issuer and TMEM owner
 // (both run converged; one elected lane issues each copy and each MMA)
 // TMEM: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B [256+D,256+2D).
@@ -379,7 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the P_t(n) that PV_t(n) reads; the tensor pipe executes in order.  For the
 // same reason a completed S_t(n+1) implies a completed PV_t(n): the softmax
 // may rescale O_t as soon as it sees its scores, and O_t's own barrier is
-// committed only once, after the tile's last PV.
+// committed only once per unit, after the tile's last PV.  The first PV of
+// the next unit (which overwrites O_t) waits for P of that unit's first
+// block, which the same softmax warps release only after they have read O_t
+// out for the epilogue.
 // A tile skips the streamed blocks outside its own visible range (with a
 // window the first block may be A's only, with causal masking the last is
 // B's only).
@@ -406,6 +418,7 @@ constexpr int kThreads2 = 320;
 
 struct Bars2 {
   uint64_t q_full;
+  uint64_t q_empty;     // the unit's score MMAs are done with Q_A, Q_B
   uint64_t k_full[4];
   uint64_t k_empty[4];  // K stage free once the S MMAs of both tiles completed
   uint64_t v_full[4];
@@ -413,13 +426,63 @@ struct Bars2 {
   uint64_t s_full[2];   // per tile
   uint64_t p_half[2];   // per tile: keys 0-63 of P stored (and O rescaled), one arrival per softmax warp
   uint64_t p_full[2];   // per tile: keys 64-127 of P stored, one arrival per softmax warp
-  uint64_t o_done[2];   // per tile: all its PV MMAs completed (committed once, after the last)
+  uint64_t o_done[2];   // per tile: all its PV MMAs of the unit completed (committed once per unit)
   uint64_t drain;
+  SchedRing sched;      // units handed from the producer to the other roles
   uint32_t tmem_base;
   int abort;
 };
 
 static_assert(sizeof(Bars2) <= 512, "two-tile barriers exceed their shared-memory slot");
+
+// One work unit of the two-tile forward: query blocks q_a, q_b of heads h_a,
+// h_b in batch b, KV head g; the visible KV block range of each tile (B is
+// empty past the end) and their union [lo, lo + nblk).
+struct Fwd2Unit {
+  int q_a, q_b, h_a, h_b, g, b;
+  int lo_a, hi_a, lo_b, hi_b;
+  bool has_b;
+  int lo, nblk;
+};
+
+// Units numbered with x (the query block, or block pair, counted from the
+// end of the sequence: longest causal work first) fastest, then head (pair),
+// then batch, so that the units in flight at any time share a KV head and
+// re-read its K/V blocks from L2 (measured on GB300: numbering x outermost,
+// which spreads the units in flight over all KV heads, made the long causal
+// workload's forward 2 % and its dK/dV 6.5 % slower).
+__device__ __forceinline__ Fwd2Unit fwd2_unit(const Shape& s, bool pack_heads, int u) {
+  const int nq = ceil_div(s.T, kBM);
+  const int nx = pack_heads ? nq : ceil_div(nq, 2);
+  const int ny = pack_heads ? s.H / 2 : s.H;
+  const int x = u % nx;
+  const int r = u / nx;
+  const int y = r % ny;
+  Fwd2Unit w;
+  w.b = r / ny;
+  // Block pairs: blocks 2j and 2j + 1 of one head; head pairs: one block of
+  // heads 2j and 2j + 1, which share a KV head when H/HKV is even, so that
+  // both tiles see the same key range.
+  w.q_a = pack_heads ? nq - 1 - x : 2 * (ceil_div(nq, 2) - 1 - x);
+  w.q_b = pack_heads ? w.q_a : w.q_a + 1;
+  w.h_a = pack_heads ? 2 * y : y;
+  w.h_b = pack_heads ? w.h_a + 1 : w.h_a;
+  w.g = w.h_a / (s.H / s.HKV);
+  w.lo_b = 1;
+  w.hi_b = 0;
+  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, w.q_a, w.lo_a, w.hi_a);
+  if (w.q_b < nq) kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, w.q_b, w.lo_b, w.hi_b);
+  w.has_b = w.lo_b <= w.hi_b;
+  w.lo = w.has_b ? imin(w.lo_a, w.lo_b) : w.lo_a;
+  const int hi = w.has_b ? imax(w.hi_a, w.hi_b) : w.hi_a;
+  w.nblk = hi - w.lo + 1;  // the adjacent tiles' ranges overlap or touch: the union is contiguous
+  return w;
+}
+
+__host__ __device__ __forceinline__ int fwd2_units(const Shape& s, bool pack_heads) {
+  const int nq = ceil_div(s.T, kBM);
+  return pack_heads ? nq * (s.H / 2) * s.B : ceil_div(nq, 2) * s.H * s.B;
+}
 
 template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads2, 1)
@@ -435,29 +498,13 @@ __global__ void __launch_bounds__(kThreads2, 1)
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nq = ceil_div(s.T, kBM);
-  const int b = blockIdx.z;
-  // The two tiles: query blocks q_a, q_b of heads h_a, h_b.  Block pairs:
-  // blocks 2j and 2j + 1 of one head; head pairs: one block of heads 2j and
-  // 2j + 1, which share a KV head when H/HKV is even, so that both tiles
-  // see the same key range.  Longest causal work first.
-  const int q_a = p.pack_heads ? nq - 1 - static_cast<int>(blockIdx.x)
-                               : 2 * (ceil_div(nq, 2) - 1 - static_cast<int>(blockIdx.x));
-  const int q_b = p.pack_heads ? q_a : q_a + 1;
-  const int h_a = p.pack_heads ? 2 * static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.y);
-  const int h_b = p.pack_heads ? h_a + 1 : h_a;
-  const int g = h_a / (s.H / s.HKV);
-  // visible KV block range of each tile (B is empty past the end)
-  int lo_a, hi_a, lo_b = 1, hi_b = 0;
-  kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, q_a, lo_a, hi_a);
-  if (q_b < nq) kv_range_for_q(s.T, s.Tk, kBM, kBN, s.causal, s.window, q_b, lo_b, hi_b);
-  const bool has_b = lo_b <= hi_b;
-  const int lo = has_b ? imin(lo_a, lo_b) : lo_a;
-  const int hi = has_b ? imax(hi_a, hi_b) : hi_a;
-  const int nblk = hi - lo + 1;  // the adjacent tiles' ranges overlap or touch: the union is contiguous
+  const bool pack = p.pack_heads != 0;
+  const int nunits = fwd2_units(s, pack);
+  const int cta = static_cast<int>(blockIdx.x);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars->k_full[i], 1);
       mbar_init(&bars->k_empty[i], 1);
@@ -471,6 +518,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
       mbar_init(&bars->o_done[t], 1);
     }
     mbar_init(&bars->drain, 1);
+    sched_init(&bars->sched, 9);  // consumers: eight softmax warps and the MMA warp
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -495,34 +543,51 @@ __global__ void __launch_bounds__(kThreads2, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
       }
-      mbar_arrive_expect_tx_e(&bars->q_full, (has_b ? 2 : 1) * C::kTileBytes);
-      for (int t = 0; t < (has_b ? 2 : 1); ++t)
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64,
-                        t ? h_b : h_a, (t ? q_b : q_a) * kBM, b);
-      int issued_k = 0, issued_v = 0;
-      for (int n = 0; n < nblk; ++n) {
-        const int st = n % C::kKStages;
-        if (n >= C::kKStages && !warp_wait(&bars->k_empty[st], ((n / C::kKStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx_e(&bars->k_full[st], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d_e(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, g, (lo + n) * kBN, b);
-        issued_k = n + 1;
-        const int sv = n % C::kVStages;
-        if (n >= C::kVStages && !warp_wait(&bars->v_empty[sv], ((n / C::kVStages) - 1) & 1, ctl, kCode)) break;
-        mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, g, (lo + n) * kBN, b);
-        issued_v = n + 1;
+      int kc = 0, vc = 0, uc = 0;  // K blocks, V blocks and units issued by this CTA
+      bool ok = true;
+      int u = cta;  // the CTA's first unit; later ones are claimed from the counter
+      for (int seq = 0; ok; ++seq) {
+        if (!(ok = sched_publish(&bars->sched, seq, u, ctl, kCode))) break;
+        if (u >= nunits) break;  // the end marker has been handed on
+        const Fwd2Unit w = fwd2_unit(s, pack, u);
+        // Q_A, Q_B of this unit once the previous unit's score MMAs are done
+        if (uc > 0 && !(ok = warp_wait(&bars->q_empty, (uc - 1) & 1, ctl, kCode))) break;
+        mbar_arrive_expect_tx_e(&bars->q_full, (w.has_b ? 2 : 1) * C::kTileBytes);
+        for (int t = 0; t < (w.has_b ? 2 : 1); ++t)
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64,
+                          t ? w.h_b : w.h_a, (t ? w.q_b : w.q_a) * kBM, w.b);
+        ++uc;
+        for (int n = 0; n < w.nblk; ++n) {
+          const int st = kc % C::kKStages;
+          if (kc >= C::kKStages && !(ok = warp_wait(&bars->k_empty[st], ((kc / C::kKStages) - 1) & 1, ctl, kCode)))
+            break;
+          mbar_arrive_expect_tx_e(&bars->k_full[st], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d_e(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
+                          c * 64, w.g, (w.lo + n) * kBN, w.b);
+          ++kc;
+          const int sv = vc % C::kVStages;
+          if (vc >= C::kVStages && !(ok = warp_wait(&bars->v_empty[sv], ((vc / C::kVStages) - 1) & 1, ctl, kCode)))
+            break;
+          mbar_arrive_expect_tx_e(&bars->v_full[sv], C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d_e(&tmV, &bars->v_full[sv], smem + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes,
+                          c * 64, w.g, (w.lo + n) * kBN, w.b);
+          ++vc;
+        }
+        // claim the next unit only now, near the end of this one, so that the
+        // CTAs that finish first take the next longest units
+        int claimed = 0;
+        if (lane == 0) claimed = sched_claim(p.sched);
+        u = __shfl_sync(0xffffffffu, claimed, 0);
       }
       if (bars->abort) {
         // let every copy already issued land before the CTA exits
-        drain_bar(&bars->q_full, 0, p.timeout_ns);
-        for (int n = imax(0, issued_k - C::kKStages); n < issued_k; ++n)
+        if (uc > 0) drain_bar(&bars->q_full, (uc - 1) & 1, p.timeout_ns);
+        for (int n = imax(0, kc - C::kKStages); n < kc; ++n)
           drain_bar(&bars->k_full[n % C::kKStages], (n / C::kKStages) & 1, p.timeout_ns);
-        for (int n = imax(0, issued_v - C::kVStages); n < issued_v; ++n)
+        for (int n = imax(0, vc - C::kVStages); n < vc; ++n)
           drain_bar(&bars->v_full[n % C::kVStages], (n / C::kVStages) & 1, p.timeout_ns);
       }
     }
@@ -531,63 +596,83 @@ __global__ void __launch_bounds__(kThreads2, 1)
     {  // the whole warp runs the loop; one elected lane issues
       constexpr uint32_t idesc_s = idesc_f32acc<F16>(128, 128, false, false);  // Q x K^T, both K-major
       constexpr uint32_t idesc_o = idesc_f32acc<F16>(128, D, false, true);     // P (TMEM) x V (MN-major)
-      int n_s[2] = {0, 0};  // S MMAs issued per tile (s_full phases)
-      int n_p[2] = {0, 0};  // PV MMAs issued per tile (p_full phases)
-      auto in_tile = [&](int t, int kb) { return t ? (lo_b <= kb && kb <= hi_b) : (lo_a <= kb && kb <= hi_a); };
-      int k_seen = -1;  // last streamed block whose K stage this thread waited for
-      auto issue_s = [&](int t, int n) -> bool {  // S_t = Q_t K_n^T
-        const int st = n % C::kKStages;
-        if (k_seen < n) {
-          if (!warp_wait(&bars->k_full[st], (n / C::kKStages) & 1, ctl, kCode)) return false;
-          tc_fence_after();
-          k_seen = n;
+      int n_p[2] = {0, 0};  // PV MMAs issued per tile so far (p_half / p_full phases)
+      int kc = 0, vc = 0, uc = 0;  // K blocks, V blocks and units consumed by this CTA
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int u = sched_next(&bars->sched, seq, ctl, kCode);
+        if (u < 0) {
+          ok = false;
+          break;
         }
-        const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
-        const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss_e(tmem + C::kTmS + t * 128, qdesc + off, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        mma_commit_e(&bars->s_full[t]);
-        ++n_s[t];
-        return true;
-      };
-      bool ok = warp_wait(&bars->q_full, 0, ctl, kCode);
-      if (ok && nblk > 0) {
-        for (int t = 0; ok && t < 2; ++t)
-          if (in_tile(t, lo)) ok = issue_s(t, 0);
-        if (ok) mma_commit_e(&bars->k_empty[0]);
-      }
-      for (int n = 0; ok && n < nblk; ++n) {
-        const int kb = lo + n;
-        const int stv = n % C::kVStages;
-        if (!(ok = warp_wait(&bars->v_full[stv], (n / C::kVStages) & 1, ctl, kCode))) break;
-        const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + stv * C::kTileBytes, C::kChunkBytes, 1024);
-        for (int t = 0; ok && t < 2; ++t) {
-          if (in_tile(t, kb)) {
-            // P arrives in two halves of 64 keys: the first half's MMAs run
-            // while the softmax still forms the second
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              if (!(ok = warp_wait(hf ? &bars->p_full[t] : &bars->p_half[t], n_p[t] & 1, ctl, kCode))) break;
-              tc_fence_after();
-#pragma unroll
-              for (int k4 = 0; k4 < kBN / 32; ++k4) {  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
-                const int kk = hf * (kBN / 32) + k4;
-                mma_ts_e(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4),
-                         idesc_o, (n_p[t] > 0 || kk > 0) ? 1u : 0u);
-              }
-            }
-            if (!ok) break;
-            if (kb == (t ? hi_b : hi_a)) mma_commit_e(&bars->o_done[t]);  // the tile's last PV
-            ++n_p[t];
+        if (u >= nunits) break;
+        const Fwd2Unit w = fwd2_unit(s, pack, u);
+        auto in_tile = [&](int t, int kb) {
+          return t ? (w.lo_b <= kb && kb <= w.hi_b) : (w.lo_a <= kb && kb <= w.hi_a);
+        };
+        int k_seen = -1;  // last block of this unit whose K stage this thread waited for
+        auto issue_s = [&](int t, int n) -> bool {  // S_t = Q_t K_n^T
+          const int kg = kc + n;
+          const int st = kg % C::kKStages;
+          if (k_seen < n) {
+            if (!warp_wait(&bars->k_full[st], (kg / C::kKStages) & 1, ctl, kCode)) return false;
+            tc_fence_after();
+            k_seen = n;
           }
-          if (n + 1 < nblk && in_tile(t, kb + 1)) ok = issue_s(t, n + 1);
+          const uint64_t qdesc = sdesc_sw128(sbase + C::kOffQ + t * C::kTileBytes, 16, 1024);
+          const uint64_t kdesc = sdesc_sw128(sbase + C::kOffK + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss_e(tmem + C::kTmS + t * 128, qdesc + off, kdesc + off, idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_e(&bars->s_full[t]);
+          return true;
+        };
+        if (!(ok = warp_wait(&bars->q_full, uc & 1, ctl, kCode))) break;
+        tc_fence_after();
+        ++uc;
+        if (w.nblk > 0) {
+          for (int t = 0; ok && t < 2; ++t)
+            if (in_tile(t, w.lo)) ok = issue_s(t, 0);
+          if (!ok) break;
+          mma_commit_e(&bars->k_empty[kc % C::kKStages]);
         }
-        if (!ok) break;
-        mma_commit_e(&bars->v_empty[stv]);
-        if (n + 1 < nblk) mma_commit_e(&bars->k_empty[(n + 1) % C::kKStages]);
+        if (w.nblk <= 1) mma_commit_e(&bars->q_empty);  // every score MMA of the unit is issued
+        for (int n = 0; ok && n < w.nblk; ++n) {
+          const int kb = w.lo + n;
+          const int vg = vc + n;
+          const int stv = vg % C::kVStages;
+          if (!(ok = warp_wait(&bars->v_full[stv], (vg / C::kVStages) & 1, ctl, kCode))) break;
+          const uint64_t vdesc = sdesc_sw128(sbase + C::kOffV + stv * C::kTileBytes, C::kChunkBytes, 1024);
+          for (int t = 0; ok && t < 2; ++t) {
+            if (in_tile(t, kb)) {
+              // P arrives in two halves of 64 keys: the first half's MMAs run
+              // while the softmax still forms the second
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                if (!(ok = warp_wait(hf ? &bars->p_full[t] : &bars->p_half[t], n_p[t] & 1, ctl, kCode))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k4 = 0; k4 < kBN / 32; ++k4) {  // P: 16 bf16 keys = 8 TMEM columns; V: 16 rows = 2048 bytes
+                  const int kk = hf * (kBN / 32) + k4;
+                  mma_ts_e(tmem + C::kTmO + t * D, tmem + C::kTmS + t * 128 + kk * 8, vdesc + ((kk * 2048) >> 4),
+                           idesc_o, (kb > (t ? w.lo_b : w.lo_a) || kk > 0) ? 1u : 0u);
+                }
+              }
+              if (!ok) break;
+              if (kb == (t ? w.hi_b : w.hi_a)) mma_commit_e(&bars->o_done[t]);  // the tile's last PV of the unit
+              ++n_p[t];
+            }
+            if (n + 1 < w.nblk && in_tile(t, kb + 1)) ok = issue_s(t, n + 1);
+          }
+          if (!ok) break;
+          if (n + 2 == w.nblk) mma_commit_e(&bars->q_empty);  // the unit's last score MMAs are issued
+          mma_commit_e(&bars->v_empty[stv]);
+          if (n + 1 < w.nblk) mma_commit_e(&bars->k_empty[(kc + n + 1) % C::kKStages]);
+        }
+        kc += w.nblk;
+        vc += w.nblk;
       }
       // every MMA this thread issued must finish before TMEM is released
       mma_commit_e(&bars->drain);
@@ -595,125 +680,137 @@ __global__ void __launch_bounds__(kThreads2, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax
-    const int t = warp >> 2;   // tile
+    const int t = warp >> 2;               // tile
     const int r = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
-    const int q = t ? q_b : q_a;
-    const int h = t ? h_b : h_a;
-    const int row = q * kBM + r;
-    int vis_lo, vis_hi;  // keys this row sees
-    visible_keys(s.T, s.Tk, s.causal, s.window, row, vis_lo, vis_hi);
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem + lane_addr + C::kTmS + t * 128;
     const uint32_t o_addr = tmem + lane_addr + C::kTmO + t * D;
     const float sl2 = p.scale_log2;
-    const int lo_own = t ? lo_b : lo_a;
-    const int nb = (t ? hi_b : hi_a) - lo_own + 1;  // 0 for a tile past the end
-    float m_run = -CUDART_INF_F;  // reference max, log2 domain
-    float l_run = 0.f;
+    int sc = 0, oc = 0;  // s_full and o_done phases this tile has waited for
     bool ok = true;
-    for (int j = 0; ok && j < nb; ++j) {
-      const int kb = lo_own + j;
-      if (!(ok = warp_wait(&bars->s_full[t], j & 1, ctl, kCode))) break;
-      tc_fence_after();
-      // The masking pre-pass stays rolled over 32-column chunks: unrolled with
-      // everything else, this softmax did not fit the instruction cache next
-      // to the other roles and ran several times slower.
-      if (block_needs_mask(s.T, s.Tk, kBM, kBN, s.causal, s.window, q, kb)) {
-        // rare (diagonal, window-edge and tail blocks): -inf over the masked
-        // scores in TMEM, so that both passes below stay mask-free
+    for (int seq = 0; ok; ++seq) {
+      const int u = sched_next(&bars->sched, seq, ctl, kCode);
+      if (u < 0) {
+        ok = false;
+        break;
+      }
+      if (u >= nunits) break;
+      const Fwd2Unit w = fwd2_unit(s, pack, u);
+      const int q = t ? w.q_b : w.q_a;
+      const int h = t ? w.h_b : w.h_a;
+      const int row = q * kBM + r;
+      int vis_lo, vis_hi;  // keys this row sees
+      visible_keys(s.T, s.Tk, s.causal, s.window, row, vis_lo, vis_hi);
+      const int lo_own = t ? w.lo_b : w.lo_a;
+      const int nb = (t ? w.hi_b : w.hi_a) - lo_own + 1;  // 0 for a tile past the end
+      float m_run = -CUDART_INF_F;  // reference max, log2 domain
+      float l_run = 0.f;
+      for (int j = 0; ok && j < nb; ++j) {
+        const int kb = lo_own + j;
+        if (!(ok = warp_wait(&bars->s_full[t], sc & 1, ctl, kCode))) break;
+        ++sc;
+        tc_fence_after();
+        // The masking pre-pass stays rolled over 32-column chunks: unrolled with
+        // everything else, this softmax did not fit the instruction cache next
+        // to the other roles and ran several times slower.
+        if (block_needs_mask(s.T, s.Tk, kBM, kBN, s.causal, s.window, q, kb)) {
+          // rare (diagonal, window-edge and tail blocks): -inf over the masked
+          // scores in TMEM, so that both passes below stay mask-free
 #pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t ra[32];
-          tmem_ld32(s_addr + c4 * 32, ra);
-          tmem_ld_wait(ra);
-          // this row's visible keys, relative to the chunk
-          const int a = vis_lo - (kb * kBN + c4 * 32), z = vis_hi - (kb * kBN + c4 * 32);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t ra[32];
+            tmem_ld32(s_addr + c4 * 32, ra);
+            tmem_ld_wait(ra);
+            // this row's visible keys, relative to the chunk
+            const int a = vis_lo - (kb * kBN + c4 * 32), z = vis_hi - (kb * kBN + c4 * 32);
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < a || c > z) ra[c] = __float_as_uint(-CUDART_INF_F);
-          tmem_st32(s_addr + c4 * 32, ra);
+            for (int c = 0; c < 32; ++c)
+              if (c < a || c > z) ra[c] = __float_as_uint(-CUDART_INF_F);
+            tmem_st32(s_addr + c4 * 32, ra);
+          }
+          tmem_st_wait();
+        }
+        // One TMEM round trip per block: the row's 128 scores stay in registers
+        // for both passes (re-reading them for pass 2 cost two more load
+        // latencies on the softmax's critical path).
+        // pass 1 rides on the loads: each 32-column load also returns the
+        // maximum of its values (sm_103a load-with-reduction)
+        uint32_t s0[32], s1[32], s2[32], s3[32];
+        float m0, m1, m2, m3;
+        tmem_ld32_max(s_addr, s0, m0);
+        tmem_ld32_max(s_addr + 32, s1, m1);
+        tmem_ld32_max(s_addr + 64, s2, m2);
+        tmem_ld32_max(s_addr + 96, s3, m3);
+        tmem_ld_wait(s0);
+        reg_tie(s1);
+        reg_tie(s2);
+        reg_tie(s3);
+        reg_tie4(m0, m1, m2, m3);
+        float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        mx *= sl2;  // scale > 0, so the max commutes with the scaling
+        const float m_new = fmaxf(m_run, mx);
+        const bool first = (j == 0);
+        const bool resc = !first && (m_new - m_run > kRescaleThreshold);
+        const float m_ref = (first || resc) ? m_new : m_run;
+        const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
+        // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
+        // 64 columns of S_t.  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
+        // - (m, m) in one instruction; the sum in two packed partials.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t sum2[2] = {0ull, 0ull};
+        // 32 scores -> 16 packed columns of P, stored as soon as they are formed
+        // so that each quarter's registers free up for the next
+        auto exp_quarter = [&](const uint32_t(&a)[32], uint32_t col) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint64_t x01 =
+                f2_fma(f2_pack(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])), sl2x2, negm2);
+            float x0, x1;
+            f2_unpack(x01, x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
+            pk[e] = pack2<F16>(p0, p1);
+          }
+          tmem_st16(s_addr + col, pk);
+        };
+        exp_quarter(s0, 0);
+        exp_quarter(s1, 16);
+        if (!first && __any_sync(0xffffffffu, resc)) {
+          // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order
+          // pipe); rescaled before the first half of P is released to PV_t(j)
+          const float corr = resc ? ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ro[32];
+            tmem_ld32(o_addr + c * 32, ro);
+            tmem_ld_wait(ro);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
+            tmem_st32(o_addr + c * 32, ro);
+          }
+          if (resc) l_run *= corr;
         }
         tmem_st_wait();
+        tc_fence_before();
+        warp_arrive(&bars->p_half[t]);
+        exp_quarter(s2, 32);
+        exp_quarter(s3, 48);
+        tmem_st_wait();
+        float a0, a1;
+        f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
+        if (first || resc) m_run = m_new;
+        l_run += a0 + a1;
+        tc_fence_before();
+        warp_arrive(&bars->p_full[t]);
       }
-      // One TMEM round trip per block: the row's 128 scores stay in registers
-      // for both passes (re-reading them for pass 2 cost two more load
-      // latencies on the softmax's critical path).
-      // pass 1 rides on the loads: each 32-column load also returns the
-      // maximum of its values (sm_103a load-with-reduction)
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      float m0, m1, m2, m3;
-      tmem_ld32_max(s_addr, s0, m0);
-      tmem_ld32_max(s_addr + 32, s1, m1);
-      tmem_ld32_max(s_addr + 64, s2, m2);
-      tmem_ld32_max(s_addr + 96, s3, m3);
-      tmem_ld_wait(s0);
-      reg_tie(s1);
-      reg_tie(s2);
-      reg_tie(s3);
-      reg_tie4(m0, m1, m2, m3);
-      float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-      mx *= sl2;  // scale > 0, so the max commutes with the scaling
-      const float m_new = fmaxf(m_run, mx);
-      const bool first = (j == 0);
-      const bool resc = !first && (m_new - m_run > kRescaleThreshold);
-      const float m_ref = (first || resc) ? m_new : m_run;
-      const float m_use = (m_ref == -CUDART_INF_F) ? 0.f : m_ref;
-      // pass 2: P = 2^(S*scale*log2e - m), row sum, bf16 pairs into the first
-      // 64 columns of S_t.  Paired fp32: (x0, x1) = (s0, s1)*scale*log2e
-      // - (m, m) in one instruction; the sum in two packed partials.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2);
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
-      uint64_t sum2[2] = {0ull, 0ull};
-      // 32 scores -> 16 packed columns of P, stored as soon as they are formed
-      // so that each quarter's registers free up for the next
-      auto exp_quarter = [&](const uint32_t(&a)[32], uint32_t col) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint64_t x01 = f2_fma(f2_pack(__uint_as_float(a[2 * e]), __uint_as_float(a[2 * e + 1])), sl2x2, negm2);
-          float x0, x1;
-          f2_unpack(x01, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          sum2[e & 1] = f2_add(sum2[e & 1], f2_pack(p0, p1));
-          pk[e] = pack2<F16>(p0, p1);
-        }
-        tmem_st16(s_addr + col, pk);
-      };
-      exp_quarter(s0, 0);
-      exp_quarter(s1, 16);
-      if (!first && __any_sync(0xffffffffu, resc)) {
-        // O_t holds P_0..P_{j-1} V, complete since S_t(j) is (in-order
-        // pipe); rescaled before the first half of P is released to PV_t(j)
-        const float corr = resc ? ex2(m_run - m_new) : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ro[32];
-          tmem_ld32(o_addr + c * 32, ro);
-          tmem_ld_wait(ro);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ro[e] = __float_as_uint(__uint_as_float(ro[e]) * corr);
-          tmem_st32(o_addr + c * 32, ro);
-        }
-        if (resc) l_run *= corr;
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive(&bars->p_half[t]);
-      exp_quarter(s2, 32);
-      exp_quarter(s3, 48);
-      tmem_st_wait();
-      float a0, a1;
-      f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
-      if (first || resc) m_run = m_new;
-      l_run += a0 + a1;
-      tc_fence_before();
-      warp_arrive(&bars->p_full[t]);
-    }
-    if (ok && nb > 0) ok = warp_wait(&bars->o_done[t], 0, ctl, kCode);
-    if (ok && nb > 0) {
+      if (!ok || nb == 0) continue;
+      if (!(ok = warp_wait(&bars->o_done[t], oc & 1, ctl, kCode))) break;
+      ++oc;
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(b) * s.T + row) * s.H + h) * s.D;
+      uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(w.b) * s.T + row) * s.H + h) * s.D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ro[32];
@@ -732,13 +829,14 @@ __global__ void __launch_bounds__(kThreads2, 1)
       }
       if (row < s.T) {
         const float lse = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994530942f : 0.f;
-        p.LSE[(static_cast<size_t>(b) * s.H + h) * s.T + row] = lse;
+        p.LSE[(static_cast<size_t>(w.b) * s.H + h) * s.T + row] = lse;
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) sched_exit(p.sched);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
@@ -756,8 +854,8 @@ cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int nq = ceil_div(p.s.T, kBM);
-  const dim3 grid = p.pack_heads ? dim3(nq, p.s.H / 2, p.s.B) : dim3(ceil_div(nq, 2), p.s.H, p.s.B);
+  const int units = fwd2_units(p.s, p.pack_heads != 0);
+  const dim3 grid(imax(1, imin(p.ctas, units)));
   fa_fwd2_bf16_kernel<D, F16><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
   return cudaGetLastError();
 }

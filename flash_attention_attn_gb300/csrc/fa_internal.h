@@ -72,6 +72,8 @@ __host__ __device__ __forceinline__ bool block_needs_mask(int Tq, int Tk, int BM
   return false;
 }
 
+struct SchedCounter;  // fa_sched.cuh: the work counter of a persistent kernel (in the workspace)
+
 struct Shape {
   int B, T, H, HKV, D;  // T: query rows
   float scale;
@@ -91,6 +93,8 @@ struct FwdParams {
   int inject_stall;
   int f16;            // elements are fp16 (else bf16)
   int pack_heads;     // two-tile kernel: the tiles are one query block of two heads (else two blocks of one head)
+  int ctas;           // persistent kernels: CTAs to launch (at most one per SM; capped by the unit count)
+  SchedCounter* sched;  // persistent kernels: their work counter in the workspace (zero between launches)
 };
 
 struct BwdParams {
@@ -105,6 +109,8 @@ struct BwdParams {
   float scale_log2;
   uint64_t timeout_ns;
   int f16;            // elements are fp16 (else bf16)
+  int ctas;           // persistent kernels: CTAs to launch (at most one per SM; capped by the unit count)
+  SchedCounter* sched;  // persistent kernels: their work counter in the workspace (zero between launches)
 };
 
 // 3-D views [B][T][heads*D] with boxes of 64 elements x R rows x 1 batch:

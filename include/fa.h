@@ -38,11 +38,13 @@
  * never accumulated into, so they need no clearing.
  *
  * Workspace.  Each call takes a caller-owned device workspace of at least
- * fa_workspace_size() bytes, 256-byte aligned.  Its first 4 bytes are the
- * device error word, which must be zero before the first call (allocate the
- * workspace zero-filled); fa_check_status() reads it and sets it back to
- * zero.  The backward also keeps Delta = rowsum(dO * O), [B, H, T] fp32, in
- * the workspace.  Calls that share a workspace must be ordered (same stream).
+ * fa_workspace_size() bytes, 256-byte aligned.  Its first 256 bytes must be
+ * zero before the first call (allocate the workspace zero-filled): they hold
+ * the device error word (the first 4 bytes), which fa_check_status() reads
+ * and sets back to zero, and the work counters of the persistent kernels,
+ * which every launch leaves at zero again.  The backward also keeps
+ * Delta = rowsum(dO * O), [B, H, T] fp32, in the workspace.  Calls that share
+ * a workspace must be ordered (same stream).
  *
  * Streams.  Every launch goes onto `stream` (a cudaStream_t; NULL = the
  * legacy default stream) and returns without synchronising.
@@ -330,6 +332,18 @@ int fa_debug_config(unsigned long long wait_timeout_ns, int inject_stall);
  * later calls of this process only.
  */
 int fa_debug_fwd_tiles(int tiles);
+
+/*
+ * Test hook.  The tensor-core forward (two-tile kernel) and both backward
+ * kernels are persistent: they launch at most one CTA per SM and each CTA
+ * walks a fixed share of the work units (query tiles, or KV blocks for
+ * dK/dV), longest first.  ctas > 0 sets the CTAs launched (at most one per
+ * work unit): fewer than the SMs sends several units through one CTA on
+ * small shapes, more gives every unit a CTA of its own; 0 restores one per
+ * SM.  Results do not depend on it.  FA_ERR_INVALID_ARG for ctas < 0.
+ * Affects later calls of this process only.
+ */
+int fa_debug_max_ctas(int ctas);
 
 /* Bit flags of the device error word (which wait gave up). */
 typedef enum {

@@ -146,6 +146,12 @@ def test_forward_tiles_hook_validates(lib):
         assert fb.fa_debug_fwd_tiles(t) == fb.FA_OK
 
 
+def test_persistent_ctas_hook_validates(lib):
+    assert fb.fa_debug_max_ctas(-1) == fb.FA_ERR_INVALID_ARG
+    for n in (1, 3, 0):
+        assert fb.fa_debug_max_ctas(n) == fb.FA_OK
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert fb.fa_status_string(code) not in ("", "unknown status")

@@ -169,6 +169,56 @@ def test_forward_tiles_per_cta(case, tiles):
     check_fwd(w, got["o"], O, got["lse"], LSE)
 
 
+PERSISTENT_CASES = [
+    # dtype, B, H, HKV, T, D, window, causal
+    ("bf16", 2, 4, 2, 300, 64, 0, True),      # head pairs, ragged tail
+    ("bf16", 1, 8, 2, 513, 128, 200, True),   # window, units of different lengths
+    ("fp16", 1, 6, 3, 700, 128, 0, True),     # odd H/HKV: block pairs in the forward
+    ("bf16", 2, 2, 2, 260, 96, 0, False),     # non-causal
+    ("bf16", 1, 4, 4, 129, 64, 1, True),      # units of one block
+]
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+@pytest.mark.parametrize("case", PERSISTENT_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_persistent_kernels_with_few_ctas(case, ctas):
+    """The persistent forward and backward kernels with their CTA count
+    capped, so that every CTA walks several work units (phases of every
+    barrier, the TMEM accumulators and the resident tiles carried from one
+    unit to the next): against the oracle element by element, and bitwise
+    equal to the run with one CTA per SM (a unit's arithmetic does not depend
+    on the CTA that runs it)."""
+    dtype, B, H, HKV, T, D, window, causal = case
+    w = Workload(106, "persistent", dtype, B, H, HKV, T, D, window, causal, True, "normal")
+    inp = make_inputs(w, seed=5000 + T + D + H + ctas)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+
+    def run():
+        o, lse = fa.attention_fwd(q, k, v, scale=w.scale, causal=causal, window=window)
+        grads = fa.attention_bwd(q, k, v, o, lse, do, scale=w.scale, causal=causal, window=window)
+        st, word = fa.check_status()
+        assert st == fa.FA_OK, f"device error word {word:#x}"
+        return (o, lse) + tuple(grads)
+
+    assert fa.fa_debug_max_ctas(ctas) == fa.FA_OK
+    try:
+        capped = run()
+    finally:
+        fa.fa_debug_max_ctas(0)
+    full = run()
+    for a, b in zip(capped, full):
+        assert torch.equal(a, b)
+    got = {n: t.float().cpu().numpy().astype(np.float64) for n, t in zip(("o", "lse", "dq", "dk", "dv"), capped)}
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    O, LSE = oracle.fwd(Q, K, V, w.scale, causal, window)
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, causal, window)
+    check_fwd(w, got["o"], O, got["lse"], LSE)
+    check_grad(w, "dQ", got["dq"], dQ)
+    check_grad(w, "dK", got["dk"], dK)
+    check_grad(w, "dV", got["dv"], dV)
+
+
 def _random_cases(n=32, seed=2026):
     """Seeded random shapes across the supported space: dtype, batch, GQA
     ratio, ragged lengths, head dims 16..128, causal or not, windows."""
