@@ -103,10 +103,10 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, int nva
 struct BwdBars {
   uint64_t res_full;
   uint64_t res_empty;  // the unit's MMAs are done with the resident tiles
-  uint64_t x_full[kStages];   // streamed stage (K in dQ) loaded
-  uint64_t x_empty[kStages];  // streamed stage (K in dQ) free
-  uint64_t v_full[kStages];   // dQ only: V stage loaded
-  uint64_t v_empty[kStages];  // dQ only: V stage free
+  uint64_t x_full[kStages];   // streamed stage loaded: Q (and dO, unless split) in dK/dV, K in dQ
+  uint64_t x_empty[kStages];  // streamed stage free
+  uint64_t v_full[kStages];   // second ring, stage loaded: dO in dK/dV (split rings), V in dQ
+  uint64_t v_empty[kStages];  // second ring, stage free
   uint64_t s_full[2];
   uint64_t dp_full[2];
   uint64_t p_full[2];   // P written back (256 compute threads)
@@ -120,14 +120,15 @@ struct BwdBars {
 
 static_assert(sizeof(BwdBars) <= 512, "backward barriers exceed their shared-memory slot");
 
-__device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count) {
+__device__ __forceinline__ void init_bars(BwdBars* bars, uint32_t x_full_count, uint32_t v_full_count,
+                                          uint32_t v_empty_count) {
   mbar_init(&bars->res_full, 1);
   mbar_init(&bars->res_empty, 1);
   for (int i = 0; i < kStages; ++i) {
     mbar_init(&bars->x_full[i], x_full_count);
     mbar_init(&bars->x_empty[i], 1);
-    mbar_init(&bars->v_full[i], 1);
-    mbar_init(&bars->v_empty[i], 1);
+    mbar_init(&bars->v_full[i], v_full_count);
+    mbar_init(&bars->v_empty[i], v_empty_count);
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bars->s_full[i], 1);
@@ -172,25 +173,41 @@ __device__ __forceinline__ uint32_t packed_slice_col128(int kk) { return (kk >> 
 // (P^T from S^T, then dS^T from dP^T) and the MMA warp queues
 //   dV(n) S^T(n+1) dK(n) dP^T(n+1) ...
 // so that each pass overlaps the MMAs of the other buffer.
+// At D = 128 the Q and dO blocks stream through rings of their own (kSplit):
+// a dO stage is free once dV(n) and the dS pass that reads its Delta rows
+// are done, a Q stage only after dK(n), and the Q ring has three stages, the
+// dO ring two.  A clock64 trace of one CTA on GB300 showed S^T(n+1) waiting
+// for its Q block with a shared two-stage ring (the block could only start
+// loading after dK(n-1)); the split rings took the long causal workload's
+// dK/dV 4 % faster.  They fill the 227 KB of shared memory exactly, so that
+// layout needs the dynamic shared memory to start 1024-byte aligned, which
+// the kernel checks.  At D = 64 a shared four-stage ring has room to spare
+// and one barrier per stage costs less.
 template <int D>
 struct DkdvTiles {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunk = 128 * kRowBytes;  // [128][64] bf16 = 16 KB
   static constexpr int kTile = kChunks * kChunk;
-  static constexpr int kStages = (D == 64) ? 4 : 2;
-  static constexpr int kOffRes0 = 0;                      // K
-  static constexpr int kOffRes1 = kTile;                  // V
-  static constexpr int kOffX = 2 * kTile;                 // Q stages
-  static constexpr int kOffY = kOffX + kStages * kTile;   // dO stages
-  static constexpr int kOffRows = kOffY + kStages * kTile;  // [stage][LSE*log2e 128 | Delta 128]
-  static constexpr int kOffBar = kOffRows + kStages * 2 * 128 * 4;
-  static constexpr int kSmemBytes = kOffBar + 512 + 1024;
+  static constexpr bool kSplit = (D == 128);
+  static constexpr int kQStages = (D == 64) ? 4 : 3;
+  static constexpr int kOStages = (D == 64) ? 4 : 2;  // equal to kQStages when the rings are shared
+  static constexpr int kOffRes0 = 0;                            // K
+  static constexpr int kOffRes1 = kTile;                        // V
+  static constexpr int kOffX = 2 * kTile;                       // Q stages
+  static constexpr int kOffY = kOffX + kQStages * kTile;        // dO stages
+  static constexpr int kOffLse = kOffY + kOStages * kTile;      // [Q stage][-LSE*log2e of 128 rows]
+  static constexpr int kOffDel = kOffLse + kQStages * 128 * 4;  // [dO stage][Delta of 128 rows]
+  static constexpr int kOffBar = kOffDel + kOStages * 128 * 4;
+  static constexpr int kSlack = kSplit ? 0 : 1024;              // room to align the base (none when split)
+  static constexpr int kSmemBytes = kOffBar + 512 + kSlack;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmS = 0;     // S^T, then P^T (bf16)
   static constexpr uint32_t kTmDP = 128;  // dP^T, then dS^T (bf16)
   static constexpr uint32_t kTmDV = 256;
   static constexpr uint32_t kTmDK = 256 + D;
+  static_assert(kSplit || kQStages == kOStages, "a shared ring has one stage count");
 };
+static_assert(DkdvTiles<128>::kSmemBytes <= 232448, "dK/dV tiles exceed 227 KB of shared memory");
 
 // Work units of the dK/dV kernel: (KV block kb, KV head g, batch b), numbered
 // with kb fastest, ascending (under causal masking the first key blocks are
@@ -207,11 +224,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = DkdvTiles<D>;
   constexpr int BQ = 128;  // query rows per streamed block
   constexpr int BK = 128;  // key rows per unit
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(C::kSlack)) {
+    // the layout does not fit: report it (FA_DEVERR_LAYOUT) and do nothing
+    if (threadIdx.x == 0) {
+      atomicOr(p.err, 8u);
+      sched_exit(p.sched);
+    }
+    return;
+  }
+  uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = smem_u32(smem);
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem + C::kOffBar);
-  float* srows = reinterpret_cast<float*>(smem + C::kOffRows);
+  float* slse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sdel = reinterpret_cast<float*>(smem + C::kOffDel);
+  // the barriers that guard a dO stage: the second ring's, or the Q stage's
+  // own when the rings are shared
+  uint64_t* const do_full = C::kSplit ? bars->v_full : bars->x_full;
 
   const Shape& s = p.s;
   const int warp = threadIdx.x >> 5;
@@ -238,7 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     return w;
   };
 
-  if (threadIdx.x == 0) init_bars(bars, 1 + 32);
+  // Q (and dO) stages: the elected lane's expect-tx plus the 32 lanes that
+  // write the stage's LSE and Delta rows; a split dO stage is freed by the
+  // dV MMAs' commit and by the eight compute warps once they have read its
+  // Delta rows
+  if (threadIdx.x == 0) init_bars(bars, 1 + 32, 1 + 32, 1 + kCompute / 32);
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();
@@ -275,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++uc;
       // -LSE (pre-scaled to base 2) and Delta of one block's 128 query rows,
       // four per lane; read one block ahead so that their latency overlaps the
-      // wait for the stage
+      // waits for the stages
       float l2[4], dl[4];
       auto load_rows = [&](int n) {
         const int h = w.g * rep + n / w.nqb;
@@ -294,25 +328,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (w.niter > 0) load_rows(0);
       for (int n = 0; n < w.niter; ++n) {
-        const int st = xc % C::kStages;
-        if (xc >= C::kStages && !(ok = warp_wait(&bars->x_empty[st], ((xc / C::kStages) - 1) & 1, ctl, kCode)))
-          break;
         const int h = w.g * rep + n / w.nqb;
         const int qb = w.qlo + n % w.nqb;
-        mbar_arrive_expect_tx_e(&bars->x_full[st], 2 * C::kTile);  // one elected lane arms and copies
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d_e(&tmQ, &bars->x_full[st], smem + C::kOffX + st * C::kTile + c * C::kChunk, c * 64, h,
+        // Q block and its -LSE*log2e rows (one elected lane arms and copies)
+        const int sq = xc % C::kQStages;
+        if (xc >= C::kQStages && !(ok = warp_wait(&bars->x_empty[sq], ((xc / C::kQStages) - 1) & 1, ctl, kCode)))
+          break;
+        mbar_arrive_expect_tx_e(&bars->x_full[sq], (C::kSplit ? 1 : 2) * C::kTile);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d_e(&tmQ, &bars->x_full[sq], smem + C::kOffX + sq * C::kTile + c * C::kChunk, c * 64, h,
                         qb * BQ, w.b);
-          tma_load_4d_e(&tmdO, &bars->x_full[st], smem + C::kOffY + st * C::kTile + c * C::kChunk, c * 64, h,
-                        qb * BQ, w.b);
-        }
-        float* rows = srows + st * 256;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          rows[lane + 32 * q4] = l2[q4];
-          rows[128 + lane + 32 * q4] = dl[q4];
+        for (int q4 = 0; q4 < 4; ++q4) slse[sq * 128 + lane + 32 * q4] = l2[q4];
+        // dO block and its Delta rows: in the Q block's stage, or in a stage
+        // of the dO ring
+        const int sd = xc % C::kOStages;
+        if (C::kSplit) {
+          mbar_arrive(&bars->x_full[sq]);
+          if (xc >= C::kOStages && !(ok = warp_wait(&bars->v_empty[sd], ((xc / C::kOStages) - 1) & 1, ctl, kCode)))
+            break;
+          mbar_arrive_expect_tx_e(&bars->v_full[sd], C::kTile);
         }
-        mbar_arrive(&bars->x_full[st]);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d_e(&tmdO, &do_full[sd], smem + C::kOffY + sd * C::kTile + c * C::kChunk, c * 64, h, qb * BQ,
+                        w.b);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) sdel[sd * 128 + lane + 32 * q4] = dl[q4];
+        mbar_arrive(&do_full[sd]);
         ++xc;
         if (n + 1 < w.niter) load_rows(n + 1);
       }
@@ -324,8 +366,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0 && bars->abort) {
       if (uc > 0) drain_bar(&bars->res_full, (uc - 1) & 1, p.timeout_ns);
-      for (int n = imax(0, xc - C::kStages); n < xc; ++n)
-        drain_bar(&bars->x_full[n % C::kStages], (n / C::kStages) & 1, p.timeout_ns);
+      for (int n = imax(0, xc - C::kQStages); n < xc; ++n)
+        drain_bar(&bars->x_full[n % C::kQStages], (n / C::kQStages) & 1, p.timeout_ns);
+      if (C::kSplit)
+        for (int n = imax(0, xc - C::kOStages); n < xc; ++n)
+          drain_bar(&bars->v_full[n % C::kOStages], (n / C::kOStages) & 1, p.timeout_ns);
     }
   } else if (warp == 9) {
     // ----------------------------------------------------------- MMA issuer
@@ -335,18 +380,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sK = sbase + C::kOffRes0;
       const uint32_t sV = sbase + C::kOffRes1;
       int xc = 0, uc = 0;  // streamed stages and units consumed (x_full, p/ds phases run with xc)
-      auto issue_s = [&](int xg) -> bool {  // S^T = K Q^T of streamed stage xg
-        const int st = xg % C::kStages;
-        if (!warp_wait(&bars->x_full[st], (xg / C::kStages) & 1, ctl, kCode)) return false;
+      auto q_ready = [&](int xg) -> bool {  // Q block xg (and its dO, when the rings are shared) loaded
+        const int sq = xg % C::kQStages;
+        if (!warp_wait(&bars->x_full[sq], (xg / C::kQStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
-        issue_kk<D>(tmem + C::kTmS, sK, C::kChunk, sbase + C::kOffX + st * C::kTile, C::kChunk, idesc_s);
-        mma_commit_e(&bars->s_full[0]);
         return true;
       };
-      auto issue_dp = [&](int xg) {  // dP^T = V dO^T (stage already waited for by issue_s)
-        issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + (xg % C::kStages) * C::kTile, C::kChunk,
-                    idesc_s);
+      auto issue_s = [&](int xg) {  // S^T = K Q^T of Q block xg (already waited for)
+        const int sq = xg % C::kQStages;
+        issue_kk<D>(tmem + C::kTmS, sK, C::kChunk, sbase + C::kOffX + sq * C::kTile, C::kChunk, idesc_s);
+        mma_commit_e(&bars->s_full[0]);
+      };
+      auto issue_dp = [&](int xg) -> bool {  // dP^T = V dO^T of dO block xg
+        const int sd = xg % C::kOStages;
+        if (C::kSplit) {
+          if (!warp_wait(&bars->v_full[sd], (xg / C::kOStages) & 1, ctl, kCode)) return false;
+          tc_fence_after();
+        }
+        issue_kk<D>(tmem + C::kTmDP, sV, C::kChunk, sbase + C::kOffY + sd * C::kTile, C::kChunk, idesc_s);
         mma_commit_e(&bars->dp_full[0]);
+        return true;
       };
       // acc (+)= A[TMEM, 128 packed query rows] x B[128 query rows][D] (MN-major)
       auto issue_acc128 = [&](uint32_t acc, uint32_t a_tmem, uint32_t b_smem, bool accumulate) {
@@ -369,23 +422,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         ++uc;
         if (w.niter > 0) {
-          if (!(ok = issue_s(xc))) break;
-          issue_dp(xc);
+          if (!(ok = q_ready(xc))) break;
+          issue_s(xc);
+          if (!(ok = issue_dp(xc))) break;
         }
         if (w.niter <= 1) mma_commit_e(&bars->res_empty);  // every MMA reading K and V is issued
         for (int n = 0; ok && n < w.niter; ++n) {
           const int xg = xc + n;
-          const int st = xg % C::kStages;
+          const int sq = xg % C::kQStages;
+          const int sd = xg % C::kOStages;
+          // the next Q block's wait while the compute warps still form P^T_n,
+          // so that S^T_{n+1} follows the dV MMAs without a gap (the deeper
+          // Q ring, or the shared four-stage one, has it loaded by then)
+          if (n + 1 < w.niter && !(ok = q_ready(xg + 1))) break;
           if (!(ok = warp_wait(&bars->p_full[0], xg & 1, ctl, kCode))) break;
           tc_fence_after();
-          issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + st * C::kTile, n > 0);  // dV += P^T dO
-          if (n + 1 < w.niter && !(ok = issue_s(xg + 1))) break;  // P^T_n is read by the dV MMAs queued above
+          issue_acc128(tmem + C::kTmDV, tmem + C::kTmS, sbase + C::kOffY + sd * C::kTile, n > 0);  // dV += P^T dO
+          if (C::kSplit) mma_commit_e(&bars->v_empty[sd]);  // the dO stage, once its Delta rows are read too
+          if (n + 1 < w.niter) issue_s(xg + 1);  // P^T_n is read by the dV MMAs queued above
           if (!(ok = warp_wait(&bars->ds_full[0], xg & 1, ctl, kCode))) break;
           tc_fence_after();
-          issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + st * C::kTile, n > 0);  // dK += dS^T Q
-          mma_commit_e(&bars->x_empty[st]);
+          issue_acc128(tmem + C::kTmDK, tmem + C::kTmDP, sbase + C::kOffX + sq * C::kTile, n > 0);  // dK += dS^T Q
+          mma_commit_e(&bars->x_empty[sq]);
           if (n + 1 < w.niter) {
-            issue_dp(xg + 1);  // dS^T_n is read by the dK MMAs queued above
+            if (!(ok = issue_dp(xg + 1))) break;  // dS^T_n is read by the dK MMAs queued above
             if (n + 2 == w.niter) mma_commit_e(&bars->res_empty);  // the unit's last MMAs reading K and V
           }
         }
@@ -418,12 +478,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = w.kb * BK + jrow;
       for (int n = 0; ok && n < w.niter; ++n) {
         const int xg = xc + n;
-        const int st = xg % C::kStages;
+        const int sq = xg % C::kQStages;
+        const int sd = xg % C::kOStages;
         const int qb = w.qlo + n % w.nqb;
-        const float* rows = srows + st * 256 + half * 64;
-        // pass 1: P^T = 2^(S^T*scale*log2e - LSE*log2e), masked -> bf16 over S^T
+        // pass 1: P^T = 2^(S^T*scale*log2e - LSE*log2e), masked -> bf16 over S^T.
+        // The stage's LSE rows land long before the scores: wait for them
+        // first, so that this wait stays off the chain from S^T to the dV MMAs.
+        if (!(ok = warp_wait(&bars->x_full[sq], (xg / C::kQStages) & 1, ctl, kCode))) break;  // LSE rows visible
         if (!(ok = warp_wait(&bars->s_full[0], xg & 1, ctl, kCode))) break;
-        if (!(ok = warp_wait(&bars->x_full[st], (xg / C::kStages) & 1, ctl, kCode))) break;  // rows visible
         tc_fence_after();
         const bool need_mask = block_needs_mask(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, w.kb);
         float pv[64];
@@ -436,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[32 + c] = hi[c];
           }
         }
-        const float4* lse4 = reinterpret_cast<const float4*>(rows);  // -LSE*log2e per query
+        const float4* lse4 = reinterpret_cast<const float4*>(slse + sq * 128 + half * 64);  // -LSE*log2e per query
         const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
@@ -470,12 +532,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&bars->p_full[0]);
-        // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T
+        // pass 2: dS^T = P^T (dP^T - Delta) -> bf16 over dP^T (the Delta rows
+        // came with the dO block, before dP^T)
+        if (C::kSplit && !(ok = warp_wait(&bars->v_full[sd], (xg / C::kOStages) & 1, ctl, kCode))) break;
         if (!(ok = warp_wait(&bars->dp_full[0], xg & 1, ctl, kCode))) break;
         tc_fence_after();
         float dlo[32], dhi[32];
         load_two_cols32(dp_addr, dp_addr + 32, dlo, dhi);
-        const float4* del4 = reinterpret_cast<const float4*>(rows + 128);
+        const float4* del4 = reinterpret_cast<const float4*>(sdel + sd * 128 + half * 64);
         uint32_t pk[32];
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
@@ -504,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         warp_arrive(&bars->ds_full[0]);
+        if (C::kSplit) warp_arrive(&bars->v_empty[sd]);  // its Delta rows are read
       }
       if (!ok) break;
       xc += w.niter;
@@ -598,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return w;
   };
 
-  if (threadIdx.x == 0) init_bars(bars, 1);
+  if (threadIdx.x == 0) init_bars(bars, 1, 1, 1);
   if (warp == 9) {
     tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tmem_relinquish();

@@ -349,7 +349,10 @@ int fa_debug_max_ctas(int ctas);
 typedef enum {
   FA_DEVERR_FWD_TIMEOUT = 1u << 0,
   FA_DEVERR_DKDV_TIMEOUT = 1u << 1,
-  FA_DEVERR_DQ_TIMEOUT = 1u << 2
+  FA_DEVERR_DQ_TIMEOUT = 1u << 2,
+  /* a kernel found its dynamic shared memory placed so that its tile layout
+     does not fit, and did nothing (fa_check_status reports FA_ERR_TIMEOUT) */
+  FA_DEVERR_LAYOUT = 1u << 3
 } fa_device_error_bits;
 
 #ifdef __cplusplus
