@@ -748,14 +748,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_e(&bars->s_full[bg & 1]);
         return true;
       };
-      auto issue_dp = [&](int bg) -> bool {  // dP = dO V^T; its V stage is free once this completes
+      auto v_ready = [&](int bg) -> bool {  // V block bg loaded
         const int st = bg % C::kVStages;
         if (!warp_wait(&bars->v_full[st], (bg / C::kVStages) & 1, ctl, kCode)) return false;
         tc_fence_after();
+        return true;
+      };
+      auto issue_dp = [&](int bg) {  // dP = dO V^T (V already waited for); its V stage is free once this completes
+        const int st = bg % C::kVStages;
         issue_kk<D>(tmem + C::kTmDP, sdO, C::kChunk, sbase + C::kOffV + st * C::kTile, C::kChunk, idesc_s);
         mma_commit_e(&bars->dp_full[0]);
         mma_commit_e(&bars->v_empty[st]);
-        return true;
       };
       int bc = 0, uc = 0;
       bool ok = true;
@@ -772,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++uc;
         if (w.nblk > 0) {
           if (!(ok = issue_s(bc))) break;
-          if (!(ok = issue_dp(bc))) break;
+          if (!(ok = v_ready(bc))) break;
+          issue_dp(bc);
         }
         if (w.nblk <= 1) mma_commit_e(&bars->res_empty);  // every MMA reading Q and dO is issued
         // queue order: S0 dP0 S1 | dP1 dQ0 S2 | dP2 dQ1 S3 ...
@@ -780,10 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int bg = bc + n;
           if (n + 1 < w.nblk && !(ok = issue_s(bg + 1))) break;
           const int st = bg % C::kKStages;
+          // the next V block's wait before the dS wait, so that dP_{n+1}
+          // issues as soon as dS_n has been written
+          if (n + 1 < w.nblk && !(ok = v_ready(bg + 1))) break;
           if (!(ok = warp_wait(&bars->ds_full[0], bg & 1, ctl, kCode))) break;
           tc_fence_after();
           if (n + 1 < w.nblk) {
-            if (!(ok = issue_dp(bg + 1))) break;  // dP_n has been read: its columns are free
+            issue_dp(bg + 1);  // dP_n has been read: its columns are free
             if (n + 2 == w.nblk) mma_commit_e(&bars->res_empty);  // the unit's last MMAs reading Q and dO
           }
           // dQ += dS K   (K = the block's 128 key rows)
