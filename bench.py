@@ -37,7 +37,7 @@ METRIC = "attention TFLOP/s fwd and fwd+bwd (causal GQA bf16) and % of BF16 tens
 DEFAULT_WORKLOAD = 5
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2**20
-KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq")
+KERNELS = ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq", "bwd_dkdv_dq")
 
 
 # ------------------------------------------------------------------ counting
@@ -62,7 +62,9 @@ def counted_flops(w: Workload) -> dict:
 
 def kernel_work(w: Workload, elem_bytes: int) -> dict:
     """Algorithmic work of one launch of each kernel (flops, or bytes for the
-    HBM-bound preprocess): forward 2 matmuls per pair, dK/dV 4, dQ 3."""
+    HBM-bound preprocess): forward 2 matmuls per pair, dK/dV 4, dQ 3, the
+    fused dK/dV + dQ 5 (dQ from the same dS tiles, without recomputing S and
+    dP)."""
     base = w.B * w.H * w.D * visible_pairs(w)
     rows = w.B * w.H * w.T
     return {
@@ -70,7 +72,21 @@ def kernel_work(w: Workload, elem_bytes: int) -> dict:
         "bwd_preprocess": ("hbm", 2.0 * rows * w.D * elem_bytes + 4.0 * rows),
         "bwd_dkdv": ("tensor", 8.0 * base),
         "bwd_dq": ("tensor", 6.0 * base),
+        "bwd_dkdv_dq": ("tensor", 10.0 * base),
     }
+
+
+def fused_backward(w: Workload) -> bool:
+    """fa_bwd runs dK, dV and dQ in one kernel (no recompute for dQ) for
+    16-bit elements, head dims up to 64 and causal masking."""
+    return w.dtype in ("bf16", "fp16") and w.D <= 64 and w.causal
+
+
+def backward_stages(w: Workload) -> list:
+    """The launches of fa_bwd for this workload, as its stage entry points."""
+    if fused_backward(w):
+        return ["bwd_preprocess", "bwd_dkdv_dq"]
+    return ["bwd_preprocess", "bwd_dkdv", "bwd_dq"]
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -98,7 +114,7 @@ def source_sha(name: str) -> str:
 
 
 KERNEL_SOURCES = {"fwd": "fa_fwd_bf16.cu", "bwd_preprocess": "fa_delta.cu",
-                  "bwd_dkdv": "fa_bwd_bf16.cu", "bwd_dq": "fa_bwd_bf16.cu"}
+                  "bwd_dkdv": "fa_bwd_bf16.cu", "bwd_dq": "fa_bwd_bf16.cu", "bwd_dkdv_dq": "fa_bwd_fused.cu"}
 
 
 def ncu_traffic(kernel: str, workload_name: str):
@@ -363,6 +379,8 @@ class _Sets:
             st = lib.fa_bwd_preprocess(o, do, *a, dt, ws, n, s)
         elif name == "bwd_dkdv":
             st = lib.fa_bwd_dkdv(q, k, v, lse, do, dk, dv, *a, sc, c, win, dt, ws, n, s)
+        elif name == "bwd_dkdv_dq":
+            st = lib.fa_bwd_dkdv_dq(q, k, v, lse, do, dq, dk, dv, *a, sc, c, win, dt, ws, n, s)
         else:
             st = lib.fa_bwd_dq(q, k, v, lse, do, dq, *a, sc, c, win, dt, ws, n, s)
         if st != 0:
@@ -407,7 +425,7 @@ def measure_workload(w: Workload, dev, peaks: dict, min_loop_ms: float = 200.0, 
     set_bytes = w.B * w.T * (w.H * (2 if w.bwd else 1) + 2 * w.HKV) * w.D * elem
     n_sets = max(1, min(2048, math.ceil(2 * L2_BYTES / set_bytes)))
     sets = _Sets(w, dev, n_sets, lib, fb)
-    stages = ["fwd"] + (["bwd_preprocess", "bwd_dkdv", "bwd_dq"] if w.bwd else [])
+    stages = ["fwd"] + (backward_stages(w) if w.bwd else [])
     stream = torch.cuda.current_stream(dev)
 
     def step(i):
@@ -514,7 +532,13 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
         check(lib.fa_bwd_dq(P[0], P[1], P[2], P[4], P[5], P[6], B, T, H, HKV, D, sc, causal, win, dt,
                             wsp, ws_bytes, s), "fa_bwd_dq")
 
-    stages = (k_fwd, k_pre, k_dkdv, k_dq)
+    def k_fused():
+        check(lib.fa_bwd_dkdv_dq(P[0], P[1], P[2], P[4], P[5], P[6], P[7], P[8], B, T, H, HKV, D, sc, causal, win,
+                                 dt, wsp, ws_bytes, s), "fa_bwd_dkdv_dq")
+
+    kernels = ["fwd"] + backward_stages(w)
+    by_name = {"fwd": k_fwd, "bwd_preprocess": k_pre, "bwd_dkdv": k_dkdv, "bwd_dq": k_dq, "bwd_dkdv_dq": k_fused}
+    stages = tuple(by_name[n] for n in kernels)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
     flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
 
@@ -527,7 +551,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
         raise RuntimeError(f"warm-up reported device error word {word:#x}")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
@@ -544,8 +568,8 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
     if st != 0:
         raise RuntimeError(f"timed region reported device error word {word:#x}")
 
-    per_kernel = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j, name in enumerate(KERNELS)}
-    step_ms = [ev[i][0].elapsed_time(ev[i][4]) for i in range(K)]
+    per_kernel = {name: [ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)] for j, name in enumerate(kernels)}
+    step_ms = [ev[i][0].elapsed_time(ev[i][len(stages)]) for i in range(K)]
     total_s = max_over_ranks(sum(step_ms) / 1e3, world)
 
     # e2e: host buffers in pinned memory, every step's copies inside the timed
@@ -563,14 +587,11 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
         sets = [(q, k, v, do) + outs0,
                 tuple(torch.empty_like(t) for t in (q, k, v, do)) + tuple(torch.empty_like(t) for t in outs0)]
 
-        def run_set(bs):
+        def run_set(bs):  # the public calls: fa_fwd, then fa_bwd
             qq, kk, vv, dd, oo, ll, gq, gk, gv = (t.data_ptr() for t in bs)
             check(lib.fa_fwd(qq, kk, vv, oo, ll, B, T, H, HKV, D, sc, causal, win, dt, wsp, ws_bytes, s), "fa_fwd")
-            check(lib.fa_bwd_preprocess(oo, dd, B, T, H, HKV, D, dt, wsp, ws_bytes, s), "fa_bwd_preprocess")
-            check(lib.fa_bwd_dkdv(qq, kk, vv, ll, dd, gk, gv, B, T, H, HKV, D, sc, causal, win, dt, wsp, ws_bytes,
-                                  s), "fa_bwd_dkdv")
-            check(lib.fa_bwd_dq(qq, kk, vv, ll, dd, gq, B, T, H, HKV, D, sc, causal, win, dt, wsp, ws_bytes, s),
-                  "fa_bwd_dq")
+            check(lib.fa_bwd(qq, kk, vv, oo, ll, dd, gq, gk, gv, B, T, H, HKV, D, sc, causal, win, dt, wsp,
+                             ws_bytes, s), "fa_bwd")
 
         def timed(pipelined, steps):
             # Uploads and downloads run on streams of their own, so that the two
@@ -653,7 +674,7 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
     if not args.no_workloads and world == 1:
         peaks, _ = load_peaks()
         side = {str(i): measure_workload(WORKLOADS[i], dev, peaks) for i in sorted(WORKLOADS) if i != w.wid}
-    return {"workloads": side, "per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
+    return {"workloads": side, "kernels": kernels, "per_kernel_ms": per_kernel, "step_ms": step_ms, "total_s": total_s, "clocks": clocks.summary(),
             "e2e": e2e, "elem_bytes": q.element_size(), "prologue": prologue}
 
 
@@ -731,7 +752,7 @@ def main():
     work = kernel_work(w, r["elem_bytes"])
     value = world * args.steps * flops["fwd_bwd"] / r["total_s"] / 1e12
     kern = {}
-    for name in KERNELS:
+    for name in r["kernels"]:
         ms = statistics.mean(r["per_kernel_ms"][name])
         bound, amount = work[name]
         if bound == "tensor":
@@ -746,7 +767,7 @@ def main():
                       "frac": achieved / peak, "work_per_launch": amount}
         if bound == "tensor":
             kern[name]["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
-    dom = max(KERNELS, key=lambda n: kern[n]["ms"])
+    dom = max(r["kernels"], key=lambda n: kern[n]["ms"])
     traffic = ncu_traffic(dom, w.name)
     roof = {"bound": kern[dom]["bound"], "achieved": kern[dom]["achieved"], "peak": kern[dom]["peak"],
             "unit": kern[dom]["unit"], "frac": kern[dom]["frac"], "traffic": traffic, "kernel": dom,
@@ -781,14 +802,14 @@ def main():
         # the other reading of "10*B*H*T^2*D": FlashAttention's count for the
         # backward alone, over the three backward kernels' time
         "bwd_only_tflops_x10": flops["fwd_bwd"] / (sum(statistics.mean(r["per_kernel_ms"][n])
-                                                     for n in KERNELS if n != "fwd") / 1e3) / 1e12,
+                                                     for n in r["kernels"] if n != "fwd") / 1e3) / 1e12,
         "peak_bf16_tflops": peaks["bf16_tflops"],
         "peak_bf16_tflops_sustained": peaks["bf16_tflops_sustained"],
         "peak_source": f"{peak_src}: pct_of_peak against the burst cuBLAS bf16 rate, _of_sustained against the "
                        "seconds-long loop under the power cap",
         "roofline": roof,
         "kernels": kern,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": len(r["kernels"]) * args.steps,
         "clocks": r["clocks"],
         "e2e": r["e2e"],
         "device": torch.cuda.get_device_name(0),

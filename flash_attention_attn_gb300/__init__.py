@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     fa_bwd,
     fa_bwd_cross,
     fa_bwd_dkdv,
+    fa_bwd_dkdv_dq,
     fa_bwd_dq,
     fa_bwd_preprocess,
     fa_check_status,

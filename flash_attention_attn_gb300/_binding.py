@@ -78,6 +78,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.fa_bwd_dkdv.restype = _i
         lib.fa_bwd_dq.argtypes = [_vp] * 6 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
         lib.fa_bwd_dq.restype = _i
+        lib.fa_bwd_dkdv_dq.argtypes = [_vp] * 8 + [_i] * 5 + [_f, _i, _i, _i, _vp, _sz, _vp]
+        lib.fa_bwd_dkdv_dq.restype = _i
         lib.fa_check_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
         lib.fa_check_status.restype = _i
         lib.fa_status_string.argtypes = [_i]
@@ -156,6 +158,12 @@ def fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, windo
               workspace, workspace_bytes, stream) -> int:
     return load().fa_bwd_dq(Q, K, V, LSE, dO, dQ, B, T, H, HKV, head_dim, scale, causal, window, dtype,
                             workspace, workspace_bytes, stream)
+
+
+def fa_bwd_dkdv_dq(Q, K, V, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype,
+                   workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd_dkdv_dq(Q, K, V, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window,
+                                 dtype, workspace, workspace_bytes, stream)
 
 
 def fa_check_status(workspace, stream) -> tuple[int, int]:

@@ -18,8 +18,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfa_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_bwd_bf16.cu", "fa_delta.cu", "fa_fp32.cu", "fa_static_scratch.cu",
-           "fa_prologue.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_bf16.cu", "fa_bwd_bf16.cu", "fa_bwd_fused.cu", "fa_delta.cu", "fa_fp32.cu",
+           "fa_static_scratch.cu", "fa_prologue.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", CSRC, "-I", INCLUDE]

@@ -70,6 +70,19 @@ int validate_shape(int B, int T, int Tk, int H, int HKV, int D, float scale, int
 
 size_t delta_bytes(int B, int T, int H) { return round_up(sizeof(float) * static_cast<size_t>(B) * H * T, 256); }
 
+// The fused backward (head dims up to 64, 16-bit elements, causal) also keeps
+// an fp32 dQ accumulator [B,T,H,D] and one turn counter per (b, h, query
+// block) in the workspace, after Delta.
+bool fused_sizes(int head_dim, int dtype) { return dtype != FA_DTYPE_FP32 && head_dim <= 64; }
+size_t acc_bytes(int B, int T, int H, int D) { return round_up(sizeof(float) * static_cast<size_t>(B) * T * H * D, 256); }
+size_t turn_bytes(int B, int T, int H) {
+  return round_up(sizeof(unsigned) * static_cast<size_t>(B) * H * fa::ceil_div(T, fa::kBM), 256);
+}
+size_t bwd_base_bytes(int B, int T, int H) { return kErrBytes + delta_bytes(B, T, H); }
+size_t bwd_full_bytes(int B, int T, int H, int D, int dtype) {
+  return bwd_base_bytes(B, T, H) + (fused_sizes(D, dtype) ? acc_bytes(B, T, H, D) + turn_bytes(B, T, H) : 0);
+}
+
 // ---------------------------------------------------------------- devices
 
 struct DeviceInfo {
@@ -159,7 +172,7 @@ extern "C" {
 size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype) {
   if (validate_shape(B, T, T, H, HKV, head_dim, 1.f, 1, 0, dtype) != FA_OK) return 0;
   if (op == FA_OP_FWD) return kErrBytes;
-  if (op == FA_OP_BWD) return kErrBytes + delta_bytes(B, T, H);
+  if (op == FA_OP_BWD) return bwd_full_bytes(B, T, H, head_dim, dtype);
   return 0;
 }
 
@@ -211,8 +224,9 @@ int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int Tk, int H,
   if (st != FA_OK) return st;
   for (int i = 0; i < nptr; ++i)
     if (!ptrs[i] || !aligned16(ptrs[i])) return FA_ERR_INVALID_ARG;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
-      workspace_bytes < fa_workspace_size(FA_OP_BWD, B, T, H, HKV, head_dim, dtype))
+  // the error word and Delta are required; the fused backward's accumulator
+  // and turn counters are used when the workspace also holds them
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < bwd_base_bytes(B, T, H))
     return FA_ERR_WORKSPACE;
   int dev;
   if ((st = device_ok(&dev)) != FA_OK) return st;
@@ -318,6 +332,62 @@ int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const
   return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype, 3), s));
 }
 
+// 4-D fp32 view [B][T][heads][D] of the dQ accumulator; boxes of 32
+// elements x 1 head x 128 rows x 1 batch, 128-byte swizzle (the layout the
+// fused kernel stages its partials in).
+int encode_acc_map(CUtensorMap* map, const float* base, int B, int T, int heads, int D) {
+  const cuuint64_t row = static_cast<cuuint64_t>(heads) * D * 4;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(T),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4, row, row * static_cast<cuuint64_t>(T)};
+  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+// dK, dV and dQ in one launch (the fused backward); Delta must be in the
+// workspace already.  FA_ERR_UNSUPPORTED if the shape does not take it,
+// FA_ERR_WORKSPACE if the workspace lacks the accumulator.
+int fused_impl(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, void* dK,
+               void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  int st = validate_shape(B, T, T, H, HKV, head_dim, scale, causal, window, dtype);
+  if (st != FA_OK) return st;
+  if (!fa::fused_backward_applies(Shape{B, T, H, HKV, head_dim, scale, causal, window, T}, dtype != FA_DTYPE_FP32))
+    return FA_ERR_UNSUPPORTED;
+  if (workspace_bytes < bwd_full_bytes(B, T, H, head_dim, dtype)) return FA_ERR_WORKSPACE;
+  const void* ptrs[] = {Q, K, V, LSE, dO, dQ, dK, dV};
+  Shape shp;
+  float* delta;
+  if ((st = bwd_prologue(ptrs, 8, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                         workspace_bytes, &shp, &delta)) != FA_OK)
+    return st;
+  int dev;
+  if ((st = device_ok(&dev)) != FA_OK) return st;
+  fa::TensorMaps tm;
+  if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
+  float* acc = reinterpret_cast<float*>(ws + bwd_base_bytes(B, T, H));
+  unsigned* turns = reinterpret_cast<unsigned*>(ws + bwd_base_bytes(B, T, H) + acc_bytes(B, T, H, head_dim));
+  CUtensorMap acc_map;
+  if ((st = encode_acc_map(&acc_map, acc, B, T, H, head_dim)) != FA_OK) return st;
+  // every launch starts its turn counters at zero (a launch that gave up on
+  // a wait may have left some advanced)
+  if (cudaMemsetAsync(turns, 0, turn_bytes(B, T, H), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  fa::BwdParams p = bwd_params(shp, LSE, delta, dQ, dK, dV, workspace, dtype, 2);
+  p.sched = sched_counter(workspace, 3);
+  p.dq_acc = acc;
+  p.turns = turns;
+  // a cooperative launch: at most one CTA per SM, all resident together
+  const int sms = g_dev[dev].sms > 0 ? g_dev[dev].sms : 1;
+  p.ctas = fa::imin(p.ctas, sms);
+  return status_of(fa::launch_bwd_fused(tm, acc_map, p, static_cast<cudaStream_t>(stream)));
+}
+
 int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,
              void* dK, void* dV, int B, int T, int Tk, int H, int HKV, int head_dim, float scale, int causal,
              int window, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
@@ -331,6 +401,12 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const f
   if (st != FA_OK) return st;
   if ((st = preprocess_impl(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
+  // head dims up to 64 under causal masking: dQ without the recompute, when
+  // the workspace holds the accumulator
+  if (Tk == T && fa::fused_backward_applies(shp, dtype != FA_DTYPE_FP32) &&
+      workspace_bytes >= bwd_full_bytes(B, T, H, head_dim, dtype))
+    return fused_impl(Q, K, V, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                      workspace_bytes, stream);
   if ((st = dkdv_impl(Q, K, V, LSE, dO, dK, dV, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
                       workspace_bytes, stream)) != FA_OK)
     return st;
@@ -373,6 +449,13 @@ int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, con
               size_t workspace_bytes, void* stream) {
   return dq_impl(Q, K, V, LSE, dO, dQ, B, T, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
                  workspace_bytes, stream);
+}
+
+int fa_bwd_dkdv_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, void* dK,
+                   void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  return fused_impl(Q, K, V, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
+                    workspace_bytes, stream);
 }
 
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE, const void* dO, void* dQ,

@@ -111,6 +111,8 @@ struct BwdParams {
   int f16;            // elements are fp16 (else bf16)
   int ctas;           // persistent kernels: CTAs to launch (at most one per SM; capped by the unit count)
   SchedCounter* sched;  // persistent kernels: their work counter in the workspace (zero between launches)
+  float* dq_acc;        // fused backward: fp32 dQ accumulator [B,T,H,D] (workspace)
+  unsigned int* turns;  // fused backward: turn counter per (b, h, query block) (workspace, zero between launches)
 };
 
 // 3-D views [B][T][heads*D] with boxes of 64 elements x R rows x 1 batch:
@@ -140,6 +142,13 @@ cudaError_t launch_qk_norm_rope_bwd(const void* dq, const void* dk, const void* 
 // two heads that share a KV head.
 int fwd_mode(const Shape& s);
 cudaError_t launch_bwd_dkdv_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
+// Backward for head dims up to 64 under causal masking (self-attention,
+// 16-bit elements): dK, dV and dQ in one kernel, dQ without the recompute of
+// S and dP (fa_bwd_fused.cu).  acc_map: 4-D fp32 view of p.dq_acc with boxes
+// of 32 elements x 1 head x 128 rows x 1 batch, 128-byte swizzle.
+bool fused_backward_applies(const Shape& s, int f16_or_bf16);
+cudaError_t launch_bwd_fused(const TensorMaps& tm, const CUtensorMap& acc_map, const BwdParams& p,
+                             cudaStream_t stream);
 cudaError_t launch_bwd_dq_bf16(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream);
 
 // Every host-side check fa_bwd makes (shape, pointers and their alignment,

@@ -37,8 +37,9 @@
  * tensor-map encoder and a few device attributes.  Outputs are overwritten,
  * never accumulated into, so they need no clearing.
  *
- * Workspace.  Each call takes a caller-owned device workspace of at least
- * fa_workspace_size() bytes, 256-byte aligned.  Its first 256 bytes must be
+ * Workspace.  Each call takes a caller-owned device workspace of
+ * fa_workspace_size() bytes (see there for the backward's minimum), 256-byte
+ * aligned.  Its first 256 bytes must be
  * zero before the first call (allocate the workspace zero-filled): they hold
  * the device error word (the first 4 bytes), which fa_check_status() reads
  * and sets back to zero, and the work counters of the persistent kernels,
@@ -94,8 +95,13 @@ typedef enum { FA_OP_FWD = 0, FA_OP_BWD = 1 } fa_op;
 
 /*
  * Bytes of device workspace fa_fwd (op = FA_OP_FWD) or fa_bwd (FA_OP_BWD)
- * needs for this shape: 256 bytes for the error word, plus, for the backward,
- * B*H*T floats of Delta (rounded up to 256 bytes).  Returns 0 for sizes that
+ * takes for this shape: 256 bytes for the error word and the persistent
+ * kernels' work counters; for the backward also B*H*T floats of Delta
+ * (rounded up to 256 bytes), and, for 16-bit elements with head_dim <= 64,
+ * the fused backward's fp32 dQ accumulator (B*T*H*head_dim floats) and turn
+ * counters (B*H*ceil(T/128) words), each rounded up to 256 bytes.  fa_bwd
+ * needs only the first two parts; with less than the full size it runs the
+ * separate dQ kernel instead of the fused backward.  Returns 0 for sizes that
  * are out of range.
  */
 size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype);
@@ -111,12 +117,17 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * Backward: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.
- * Runs three kernels in stream order: Delta = rowsum(dO * O) into the
- * workspace, then dK/dV (one CTA per KV block, private accumulation, no
- * atomics), then dQ (one CTA per query block, fixed order, no atomics, so
- * the result is bitwise reproducible).
+ * Runs in stream order: Delta = rowsum(dO * O) into the workspace, then
+ *   - in general: dK/dV (every KV block accumulated privately by one unit of
+ *     work, no atomics), then dQ (every query block by one unit, fixed
+ *     order, no atomics);
+ *   - for 16-bit elements, head_dim <= 64, causal masking, when the workspace
+ *     has the full fa_workspace_size: one fused kernel (fa_bwd_dkdv_dq) that
+ *     forms dQ from the same dS tiles as dK, without recomputing S and dP,
+ *     adding the partials of each query block in a fixed order.
+ * Either way the result is bitwise reproducible.
  *   O, LSE: exactly what fa_fwd produced for the same inputs.
- *   workspace >= fa_workspace_size(FA_OP_BWD, ...).
+ *   workspace: at least 256 bytes plus the Delta rows (see fa_workspace_size).
  */
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
            const void* dO, void* dQ, void* dK, void* dV,
@@ -140,6 +151,27 @@ int fa_bwd_dkdv(const void* Q, const void* K, const void* V, const float* LSE, c
 int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ,
               int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The fused second stage of the backward (Graphcore
+ * flash_attention_qkv_packed.cpp, flashAttentionQKVPackedGrad: dQ_i += dS K_j
+ * written back in the same pass over KV blocks that produces dK and dV):
+ * dK, dV and dQ in one persistent, cooperatively launched kernel, after
+ * fa_bwd_preprocess.  Every (KV block, KV head, batch) unit forms, besides
+ * its dK/dV contribution, the dQ partial dS K of each query block it sees and
+ * adds it into the workspace's fp32 accumulator once the partials of the KV
+ * blocks above it are in (a turn counter per query block; the diagonal block
+ * first), so the sum has a fixed order; the last partial of a query block
+ * writes dQ = scale * accumulator in the element type.
+ *   Shapes: 16-bit elements, head_dim <= 64, causal = 1, any window; else
+ *   FA_ERR_UNSUPPORTED.  workspace >= fa_workspace_size(FA_OP_BWD, ...) (the
+ *   accumulator and turn counters included), else FA_ERR_WORKSPACE.
+ *   A turn wait is bounded like every kernel wait (FA_ERR_TIMEOUT through
+ *   fa_check_status, FA_DEVERR_DKDV_TIMEOUT in the error word).
+ */
+int fa_bwd_dkdv_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, void* dK,
+                   void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
+                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Cross-attention: fa_fwd / fa_bwd for Tq query rows over Tk key rows, no
@@ -185,8 +217,10 @@ int fa_bwd_cross(const void* Q, const void* K, const void* V, const void* O, con
  *     unwritten.  Pass a word whenever the outputs matter.
  *   No allocation: the call makes no cudaMalloc/cudaFree or other allocating
  *     call; it only issues a 4-byte memset (clearing the error word, since
- *     the array keeps the previous call's contents), the three backward
- *     kernels, and, with err_word, a 4-byte device-to-device copy.
+ *     the array keeps the previous call's contents), the backward's kernels
+ *     (when the array also has room for the fused backward's accumulator,
+ *     that path, with its memset of the turn counters), and, with err_word,
+ *     a 4-byte device-to-device copy.
  *   Validation: every check of fa_bwd runs before anything is queued, so a
  *     call that fails it launches nothing.
  *   Set-up: the first call on each device looks the array's device address

@@ -53,6 +53,37 @@ def test_workspace_sizes(lib):
     assert fb.fa_workspace_size(fb.FA_OP_BWD, 2, 1000, 8, 2, 128, 3) == 0
 
 
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("D", [16, 48, 64])
+def test_workspace_sizes_of_the_fused_backward(lib, D):
+    """16-bit elements with head dims up to 64: the backward workspace also
+    holds the fused path's fp32 dQ accumulator [B,T,H,D] and one turn counter
+    per (b, h, 128-row query block), each rounded up to 256 bytes."""
+    B, T, H, HKV = 2, 1000, 8, 2
+    want = 256 + _r256(4 * B * H * T) + _r256(4 * B * T * H * D) + _r256(4 * B * H * ((T + 127) // 128))
+    for dt in (fb.FA_DTYPE_BF16, fb.FA_DTYPE_FP16):
+        assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, D, dt) == want
+    # fp32 and wider heads keep the Delta-only layout
+    assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, 64, fb.FA_DTYPE_FP32) == 256 + _r256(4 * B * H * T)
+    assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, 72, fb.FA_DTYPE_BF16) == 256 + _r256(4 * B * H * T)
+
+
+def test_fused_backward_validation(lib):
+    """fa_bwd_dkdv_dq refuses shapes it does not take and a workspace without
+    the accumulator, before touching the device."""
+    p = [FAKE] * 8
+    full = fb.fa_workspace_size(fb.FA_OP_BWD, 1, 300, 4, 2, 64, fb.FA_DTYPE_BF16)
+    args = (1, 300, 4, 2)
+    call = lambda D, causal, dt, ws_bytes: fb.fa_bwd_dkdv_dq(*p, *args, D, 0.125, causal, 0, dt, FAKE, ws_bytes, None)
+    assert call(64, 0, fb.FA_DTYPE_BF16, full) == fb.FA_ERR_UNSUPPORTED   # not causal
+    assert call(128, 1, fb.FA_DTYPE_BF16, 1 << 30) == fb.FA_ERR_UNSUPPORTED  # head dim above 64
+    assert call(64, 1, fb.FA_DTYPE_FP32, 1 << 30) == fb.FA_ERR_UNSUPPORTED  # fp32
+    assert call(64, 1, fb.FA_DTYPE_BF16, full - 256) == fb.FA_ERR_WORKSPACE  # no room for the accumulator
+
+
 FAKE = 0x10000  # aligned, never dereferenced: validation fails first
 
 

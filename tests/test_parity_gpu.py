@@ -318,17 +318,78 @@ def test_cross_attention_rejects_masks():
         assert e.value.status == fa.FA_ERR_UNSUPPORTED
 
 
-def test_backward_is_bitwise_reproducible():
-    w = Workload(101, "repro", "bf16", 1, 8, 2, 640, 128, 0, True, True, "normal")
+@pytest.mark.parametrize("D,window", [(128, 0), (64, 0), (64, 200), (32, 0)], ids=["d128", "d64", "d64-window", "d32"])
+def test_backward_is_bitwise_reproducible(D, window):
+    """Repeated backwards give identical bits: the separate dQ kernel (D = 128)
+    and the fused one, whose dQ partials from different SMs are added in a
+    fixed order (D <= 64), with the default CTA count and with fewer CTAs."""
+    w = Workload(101, "repro", "bf16", 1, 8, 2, 640, D, window, True, True, "normal")
     inp = make_inputs(w, seed=7)
     dev = torch.device("cuda", 0)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
-    o, lse = fa.attention_fwd(q, k, v, causal=True)
-    g1 = fa.attention_bwd(q, k, v, o, lse, do, causal=True)
-    g2 = fa.attention_bwd(q, k, v, o, lse, do, causal=True)
-    torch.cuda.synchronize()
-    for a, b in zip(g1, g2):
-        assert torch.equal(a, b)
+    o, lse = fa.attention_fwd(q, k, v, causal=True, window=window)
+    g1 = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=window)
+    g2 = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=window)
+    assert fa.fa_debug_max_ctas(5) == fa.FA_OK
+    try:
+        g3 = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=window)
+    finally:
+        fa.fa_debug_max_ctas(0)
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, hex(word)
+    for a, b, c in zip(g1, g2, g3):
+        assert torch.equal(a, b) and torch.equal(a, c)
+
+
+FUSED_CASES = [
+    # dtype, B, H, HKV, T, D, window
+    ("bf16", 2, 4, 2, 300, 64, 0),     # ragged tail, GQA
+    ("bf16", 1, 8, 1, 1024, 64, 0),    # GQA 8:1, eight query blocks, up to eight partials per block
+    ("fp16", 1, 4, 4, 513, 64, 200),   # window: partials from at most three KV blocks
+    ("bf16", 1, 2, 2, 129, 32, 0),     # a one-row last block, head dim 32
+    ("bf16", 3, 2, 1, 1, 64, 0),       # T = 1
+    ("bf16", 1, 4, 2, 700, 48, 1),     # window 1: dQ = 0
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_fused_backward_against_separate_kernels_and_oracle(case):
+    """The fused backward (fa_bwd_dkdv_dq: dQ from the dK/dV kernel's dS
+    tiles, partials added in a fixed order) and the separate dK/dV and dQ
+    kernels, through the stage entry points on the same Delta: dK and dV are
+    the same kernels' arithmetic and must agree bit for bit; dQ, summed in a
+    different order, agrees with the oracle at the parity tolerance."""
+    dtype, B, H, HKV, T, D, window = case
+    w = Workload(107, "fused", dtype, B, H, HKV, T, D, window, True, True, "normal")
+    inp = make_inputs(w, seed=6000 + T + D + H)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, scale=w.scale, causal=True, window=window)
+    dt = fa.FA_DTYPE_BF16 if dtype == "bf16" else fa.FA_DTYPE_FP16
+    n = fa.fa_workspace_size(fa.FA_OP_BWD, B, T, H, HKV, D, dt)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    P = [t.data_ptr() for t in (q, k, v, o, lse, do)]
+    outs = {}
+    for path in ("separate", "fused"):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        assert fa.fa_bwd_preprocess(P[3], P[5], B, T, H, HKV, D, dt, ws.data_ptr(), n, s) == fa.FA_OK
+        args = (B, T, H, HKV, D, w.scale, 1, window, dt, ws.data_ptr(), n, s)
+        if path == "separate":
+            assert fa.fa_bwd_dkdv(P[0], P[1], P[2], P[4], P[5], dk.data_ptr(), dv.data_ptr(), *args) == fa.FA_OK
+            assert fa.fa_bwd_dq(P[0], P[1], P[2], P[4], P[5], dq.data_ptr(), *args) == fa.FA_OK
+        else:
+            assert fa.fa_bwd_dkdv_dq(P[0], P[1], P[2], P[4], P[5], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                     *args) == fa.FA_OK
+        st, word = fa.fa_check_status(ws.data_ptr(), s)
+        assert st == fa.FA_OK, hex(word)
+        outs[path] = (dq, dk, dv)
+    assert torch.equal(outs["separate"][1], outs["fused"][1]), "dK"
+    assert torch.equal(outs["separate"][2], outs["fused"][2]), "dV"
+    Q, K, V, dO = (as_f64(inp[n]) for n in ("q", "k", "v", "do"))
+    dQ, _, _, _ = oracle.bwd(Q, K, V, dO, w.scale, True, window)
+    for path in ("separate", "fused"):
+        check_grad(w, f"dQ ({path})", outs[path][0].float().cpu().numpy().astype(np.float64), dQ)
 
 
 def test_every_output_element_is_written():

@@ -44,11 +44,15 @@ def test_stalled_forward_times_out_and_recovers():
     assert np.max(np.abs(lse.cpu().numpy() - L)) <= 1e-3
 
 
-@pytest.mark.parametrize("kind,bit", [(2, 2), (3, 4)], ids=["dkdv", "dq"])
-def test_stalled_backward_kernel_times_out_and_recovers(kind, bit):
+@pytest.mark.parametrize("kind,bit,D", [(2, 2, 128), (3, 4, 128), (2, 2, 64)], ids=["dkdv", "dq", "fused"])
+def test_stalled_backward_kernel_times_out_and_recovers(kind, bit, D):
+    """The dK/dV kernel and the dQ kernel (head dim 128), and the fused
+    dK/dV + dQ kernel (head dim 64, which takes the dK/dV hook): the stalled
+    kernel gives up, reports only its own bit, and the next backward -- the
+    fused one with its turn counters reset -- is correct."""
     from flash_attention_attn_gb300.build import build
     build()
-    w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, 64, 0, True, True, "normal")
+    w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, D, 0, True, True, "normal")
     inp = make_inputs(w, seed=4)
     dev = torch.device("cuda", 0)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
