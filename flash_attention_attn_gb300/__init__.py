@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     FA_ERR_WORKSPACE,
     FA_OK,
     FA_OP_BWD,
+    FA_OP_BWD_FUSED,
     FA_OP_FWD,
     FaError,
     attention_bwd,

@@ -32,6 +32,7 @@ FA_DTYPE_FP32 = 1
 FA_DTYPE_FP16 = 2
 FA_OP_FWD = 0
 FA_OP_BWD = 1
+FA_OP_BWD_FUSED = 2
 
 _lib = None
 _lock = threading.Lock()

@@ -172,7 +172,8 @@ extern "C" {
 size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype) {
   if (validate_shape(B, T, T, H, HKV, head_dim, 1.f, 1, 0, dtype) != FA_OK) return 0;
   if (op == FA_OP_FWD) return kErrBytes;
-  if (op == FA_OP_BWD) return bwd_full_bytes(B, T, H, head_dim, dtype);
+  if (op == FA_OP_BWD) return bwd_base_bytes(B, T, H);
+  if (op == FA_OP_BWD_FUSED) return fused_sizes(head_dim, dtype) ? bwd_full_bytes(B, T, H, head_dim, dtype) : 0;
   return 0;
 }
 
@@ -224,8 +225,8 @@ int bwd_prologue(const void* const* ptrs, int nptr, int B, int T, int Tk, int H,
   if (st != FA_OK) return st;
   for (int i = 0; i < nptr; ++i)
     if (!ptrs[i] || !aligned16(ptrs[i])) return FA_ERR_INVALID_ARG;
-  // the error word and Delta are required; the fused backward's accumulator
-  // and turn counters are used when the workspace also holds them
+  // the error word and Delta (the fused backward checks for its accumulator
+  // and turn counters itself)
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < bwd_base_bytes(B, T, H))
     return FA_ERR_WORKSPACE;
   int dev;
@@ -401,12 +402,6 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const f
   if (st != FA_OK) return st;
   if ((st = preprocess_impl(O, dO, B, T, H, HKV, head_dim, dtype, workspace, workspace_bytes, stream)) != FA_OK)
     return st;
-  // head dims up to 64 under causal masking: dQ without the recompute, when
-  // the workspace holds the accumulator
-  if (Tk == T && fa::fused_backward_applies(shp, dtype != FA_DTYPE_FP32) &&
-      workspace_bytes >= bwd_full_bytes(B, T, H, head_dim, dtype))
-    return fused_impl(Q, K, V, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, workspace,
-                      workspace_bytes, stream);
   if ((st = dkdv_impl(Q, K, V, LSE, dO, dK, dV, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
                       workspace_bytes, stream)) != FA_OK)
     return st;

@@ -54,14 +54,14 @@ constexpr int kRowB = 128;  // one 64-element 16-bit row of a swizzled chunk
 
 struct FusedTiles {
   static constexpr int kChunk = 128 * kRowB;  // [128][64] 16-bit = 16 KB
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kChunk;
   static constexpr int kOffX = 2 * kChunk;                    // Q stages
   static constexpr int kOffY = kOffX + kStages * kChunk;      // dO stages
   static constexpr int kOffDS = kOffY + kStages * kChunk;     // dS: 2 chunks [128 keys][64 queries]
-  static constexpr int kOffStg = kOffDS + 2 * kChunk;         // dQ partial: 2 chunks [128 queries][32 fp32]
-  static constexpr int kOffRows = kOffStg + 2 * kChunk;       // [stage][-LSE*log2e 128 | Delta 128]
+  static constexpr int kOffStg = kOffDS + 2 * kChunk;         // dQ partials: 2 buffers x 2 chunks [128 queries][32 fp32]
+  static constexpr int kOffRows = kOffStg + 4 * kChunk;       // [stage][-LSE*log2e 128 | Delta 128]
   static constexpr int kOffBar = kOffRows + kStages * 256 * 4;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -79,8 +79,8 @@ struct FusedBars {
   uint64_t s_full, dp_full, p_full, ds_full;
   uint64_t acc_full;   // dK, dV of the unit complete
   uint64_t dq_full;    // the dQ partial of a block complete
-  uint64_t stg_full;   // the compute warps have copied it to shared memory
-  uint64_t stg_empty;  // the reducer has handed it to the TMA unit
+  uint64_t stg_full[2];   // the compute warps have copied a partial to shared memory
+  uint64_t stg_empty[2];  // the reducer has handed it to the TMA unit
   uint64_t drain;
   SchedRing sched;
   uint32_t tmem_base;
@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     mbar_init(&bars->ds_full, kComputeF / 32);
     mbar_init(&bars->acc_full, 1);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->stg_full, kComputeF / 32);
-    mbar_init(&bars->stg_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->stg_full[i], kComputeF / 32);
+      mbar_init(&bars->stg_empty[i], 1);
+    }
     mbar_init(&bars->drain, 1);
     sched_init(&bars->sched, 10);  // compute warps, MMA warp, reducer
     bars->abort = 0;
@@ -420,7 +422,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         kv_range_for_q(s.T, s.Tk, BQ, BK, s.causal, s.window, qb, kb_lo, kb_hi);
         const unsigned idx = static_cast<unsigned>(kb_hi - w.kb);
         unsigned* turn = turns + (static_cast<size_t>(w.b) * s.H + h) * nq + qb;
-        if (!(ok = warp_wait(&bars->stg_full, xg & 1, ctl, kCode))) break;
+        const int sb = xg & 1;  // staging buffer of this partial
+        if (!(ok = warp_wait(&bars->stg_full[sb], (xg >> 1) & 1, ctl, kCode))) break;
         if (idx > 0) {  // every contribution before this one must be in
           bool seen = false;
           if (lane == 0) {
@@ -436,7 +439,6 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 atomicOr(ctl.err, kCode);
                 break;
               }
-              __nanosleep(64);
             }
           }
           if (!(ok = __shfl_sync(0xffffffffu, seen, 0))) break;
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         if (lane == 0) {
           fence_async_global();
           for (int c = 0; c < 2; ++c) {
-            const void* src = smem + C::kOffStg + c * C::kChunk;
+            const void* src = smem + C::kOffStg + (2 * sb + c) * C::kChunk;
             if (idx == 0)
               tma_store_4d(&tmAcc, src, c * 32, h, qb * BQ, w.b);
             else
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           }
           bulk_commit();
           bulk_wait_read0();
-          mbar_arrive(&bars->stg_empty);  // the partial has been read out of shared memory
+          mbar_arrive(&bars->stg_empty[sb]);  // the partial has been read out of shared memory
           bulk_wait0();                   // and added into the accumulator
           fence_async_global();
           __threadfence();
@@ -500,23 +502,25 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     const uint32_t dp_addr = tmem + lane_addr + C::kTmDP + half * 64;
     const float sl2 = p.scale_log2;
     uint8_t* ds_chunk = smem + C::kOffDS + half * C::kChunk;
-    uint8_t* stg_chunk = smem + C::kOffStg + half * C::kChunk;
+    uint8_t* stg_chunk = smem + C::kOffStg + half * C::kChunk;  // + 2 chunks for the second buffer
     int xc = 0, uc = 0;
     // The dQ partial of block xg: TMEM -> shared memory for the reducer.  Run
     // in the next block's dS pass, after that block's dS is formed (its P
     // registers are dead by then) and before dS is released: releasing it
     // lets the MMA warp issue the next partial into the same TMEM columns.
     auto copy_dq = [&](int xg) -> bool {
+      const int sb = xg & 1;
       if (!warp_wait(&bars->dq_full, xg & 1, ctl, kCode)) return false;
-      if (xg > 0 && !warp_wait(&bars->stg_empty, (xg - 1) & 1, ctl, kCode)) return false;
+      // the buffer's previous partial (two blocks back) handed on
+      if (xg >= 2 && !warp_wait(&bars->stg_empty[sb], ((xg >> 1) - 1) & 1, ctl, kCode)) return false;
       tc_fence_after();
       uint32_t r[32];
       tmem_ld32(tmem + lane_addr + C::kTmDQ + half * 32, r);
       tmem_ld_wait(r);
-      store_row128_sw(stg_chunk, jrow, r);
+      store_row128_sw(stg_chunk + sb * 2 * C::kChunk, jrow, r);
       fence_async_smem();
       tc_fence_before();
-      warp_arrive(&bars->stg_full);
+      warp_arrive(&bars->stg_full[sb]);
       return true;
     };
     bool ok = true;

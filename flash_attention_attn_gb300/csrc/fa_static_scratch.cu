@@ -95,9 +95,7 @@ extern "C" int fa_bwd_static_scratch(const void* Q, const void* K, const void* V
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The array keeps whatever the previous call left: the error word must
-  // start at zero for this call (Delta and, on the fused path, the dQ
-  // accumulator are fully rewritten before they are read, and the fused
-  // path clears its turn counters itself).
+  // start at zero for this call (Delta is fully rewritten before it is read).
   if (cudaMemsetAsync(ws, 0, sizeof(unsigned int), s) != cudaSuccess) return FA_ERR_CUDA;
   st = fa_bwd(Q, K, V, O, LSE, dO, dQ, dK, dV, B, T, H, HKV, head_dim, scale, causal, window, dtype, ws,
               kScratchBytes, stream);

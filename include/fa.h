@@ -37,9 +37,8 @@
  * tensor-map encoder and a few device attributes.  Outputs are overwritten,
  * never accumulated into, so they need no clearing.
  *
- * Workspace.  Each call takes a caller-owned device workspace of
- * fa_workspace_size() bytes (see there for the backward's minimum), 256-byte
- * aligned.  Its first 256 bytes must be
+ * Workspace.  Each call takes a caller-owned device workspace of at least
+ * fa_workspace_size() bytes, 256-byte aligned.  Its first 256 bytes must be
  * zero before the first call (allocate the workspace zero-filled): they hold
  * the device error word (the first 4 bytes), which fa_check_status() reads
  * and sets back to zero, and the work counters of the persistent kernels,
@@ -91,18 +90,17 @@ typedef enum {
 
 typedef enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP32 = 1, FA_DTYPE_FP16 = 2 } fa_dtype;
 
-typedef enum { FA_OP_FWD = 0, FA_OP_BWD = 1 } fa_op;
+typedef enum { FA_OP_FWD = 0, FA_OP_BWD = 1, FA_OP_BWD_FUSED = 2 } fa_op;
 
 /*
- * Bytes of device workspace fa_fwd (op = FA_OP_FWD) or fa_bwd (FA_OP_BWD)
- * takes for this shape: 256 bytes for the error word and the persistent
- * kernels' work counters; for the backward also B*H*T floats of Delta
- * (rounded up to 256 bytes), and, for 16-bit elements with head_dim <= 64,
- * the fused backward's fp32 dQ accumulator (B*T*H*head_dim floats) and turn
- * counters (B*H*ceil(T/128) words), each rounded up to 256 bytes.  fa_bwd
- * needs only the first two parts; with less than the full size it runs the
- * separate dQ kernel instead of the fused backward.  Returns 0 for sizes that
- * are out of range.
+ * Bytes of device workspace for this shape: fa_fwd (op = FA_OP_FWD) takes
+ * 256 bytes, for the error word and the persistent kernels' work counters;
+ * fa_bwd and its stages (FA_OP_BWD) also B*H*T floats of Delta (rounded up to
+ * 256 bytes); the fused backward fa_bwd_dkdv_dq (FA_OP_BWD_FUSED, 16-bit
+ * elements with head_dim <= 64 only, else 0) also its fp32 dQ accumulator
+ * (B*T*H*head_dim floats) and turn counters (B*H*ceil(T/128) words), each
+ * rounded up to 256 bytes.  A FA_OP_BWD_FUSED workspace serves every
+ * backward entry point.  Returns 0 for sizes that are out of range.
  */
 size_t fa_workspace_size(int op, int B, int T, int H, int HKV, int head_dim, int dtype);
 
@@ -117,17 +115,13 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * Backward: dQ, dK, dV from Q, K, V, the forward's O and LSE, and dO.
- * Runs in stream order: Delta = rowsum(dO * O) into the workspace, then
- *   - in general: dK/dV (every KV block accumulated privately by one unit of
- *     work, no atomics), then dQ (every query block by one unit, fixed
- *     order, no atomics);
- *   - for 16-bit elements, head_dim <= 64, causal masking, when the workspace
- *     has the full fa_workspace_size: one fused kernel (fa_bwd_dkdv_dq) that
- *     forms dQ from the same dS tiles as dK, without recomputing S and dP,
- *     adding the partials of each query block in a fixed order.
- * Either way the result is bitwise reproducible.
+ * Runs three kernels in stream order: Delta = rowsum(dO * O) into the
+ * workspace, then dK/dV (every KV block accumulated privately by one unit of
+ * work, no atomics), then dQ (every query block by one unit, fixed order, no
+ * atomics), so the result is bitwise reproducible.  (fa_bwd_dkdv_dq is the
+ * alternative second stage that forms dQ without recomputing S and dP.)
  *   O, LSE: exactly what fa_fwd produced for the same inputs.
- *   workspace: at least 256 bytes plus the Delta rows (see fa_workspace_size).
+ *   workspace >= fa_workspace_size(FA_OP_BWD, ...).
  */
 int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const float* LSE,
            const void* dO, void* dQ, void* dK, void* dV,
@@ -164,10 +158,15 @@ int fa_bwd_dq(const void* Q, const void* K, const void* V, const float* LSE, con
  * first), so the sum has a fixed order; the last partial of a query block
  * writes dQ = scale * accumulator in the element type.
  *   Shapes: 16-bit elements, head_dim <= 64, causal = 1, any window; else
- *   FA_ERR_UNSUPPORTED.  workspace >= fa_workspace_size(FA_OP_BWD, ...) (the
- *   accumulator and turn counters included), else FA_ERR_WORKSPACE.
- *   A turn wait is bounded like every kernel wait (FA_ERR_TIMEOUT through
- *   fa_check_status, FA_DEVERR_DKDV_TIMEOUT in the error word).
+ *   FA_ERR_UNSUPPORTED.  workspace >= fa_workspace_size(FA_OP_BWD_FUSED,
+ *   ...), else FA_ERR_WORKSPACE; its turn counters are cleared by a memset
+ *   on `stream` before the launch.  A turn wait is bounded like every kernel
+ *   wait (FA_ERR_TIMEOUT through fa_check_status, FA_DEVERR_DKDV_TIMEOUT in
+ *   the error word).
+ *   Speed: measured on GB300 it is slower than fa_bwd_dkdv + fa_bwd_dq (the
+ *   recompute of S and dP costs less than handing every partial through
+ *   memory in a fixed order, whose hops between SMs are serial per query
+ *   block), so fa_bwd does not use it.
  */
 int fa_bwd_dkdv_dq(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, void* dK,
                    void* dV, int B, int T, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype,
@@ -217,10 +216,8 @@ int fa_bwd_cross(const void* Q, const void* K, const void* V, const void* O, con
  *     unwritten.  Pass a word whenever the outputs matter.
  *   No allocation: the call makes no cudaMalloc/cudaFree or other allocating
  *     call; it only issues a 4-byte memset (clearing the error word, since
- *     the array keeps the previous call's contents), the backward's kernels
- *     (when the array also has room for the fused backward's accumulator,
- *     that path, with its memset of the turn counters), and, with err_word,
- *     a 4-byte device-to-device copy.
+ *     the array keeps the previous call's contents), the three backward
+ *     kernels, and, with err_word, a 4-byte device-to-device copy.
  *   Validation: every check of fa_bwd runs before anything is queued, so a
  *     call that fails it launches nothing.
  *   Set-up: the first call on each device looks the array's device address

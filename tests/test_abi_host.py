@@ -59,23 +59,25 @@ def _r256(x):
 
 @pytest.mark.parametrize("D", [16, 48, 64])
 def test_workspace_sizes_of_the_fused_backward(lib, D):
-    """16-bit elements with head dims up to 64: the backward workspace also
-    holds the fused path's fp32 dQ accumulator [B,T,H,D] and one turn counter
-    per (b, h, 128-row query block), each rounded up to 256 bytes."""
+    """FA_OP_BWD_FUSED (16-bit elements, head dims up to 64): the backward's
+    workspace plus the fused path's fp32 dQ accumulator [B,T,H,D] and one turn
+    counter per (b, h, 128-row query block), each rounded up to 256 bytes."""
     B, T, H, HKV = 2, 1000, 8, 2
-    want = 256 + _r256(4 * B * H * T) + _r256(4 * B * T * H * D) + _r256(4 * B * H * ((T + 127) // 128))
+    base = 256 + _r256(4 * B * H * T)
+    want = base + _r256(4 * B * T * H * D) + _r256(4 * B * H * ((T + 127) // 128))
     for dt in (fb.FA_DTYPE_BF16, fb.FA_DTYPE_FP16):
-        assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, D, dt) == want
-    # fp32 and wider heads keep the Delta-only layout
-    assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, 64, fb.FA_DTYPE_FP32) == 256 + _r256(4 * B * H * T)
-    assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, 72, fb.FA_DTYPE_BF16) == 256 + _r256(4 * B * H * T)
+        assert fb.fa_workspace_size(fb.FA_OP_BWD_FUSED, B, T, H, HKV, D, dt) == want
+        assert fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, D, dt) == base
+    # the fused path takes neither fp32 nor wider heads
+    assert fb.fa_workspace_size(fb.FA_OP_BWD_FUSED, B, T, H, HKV, 64, fb.FA_DTYPE_FP32) == 0
+    assert fb.fa_workspace_size(fb.FA_OP_BWD_FUSED, B, T, H, HKV, 72, fb.FA_DTYPE_BF16) == 0
 
 
 def test_fused_backward_validation(lib):
     """fa_bwd_dkdv_dq refuses shapes it does not take and a workspace without
     the accumulator, before touching the device."""
     p = [FAKE] * 8
-    full = fb.fa_workspace_size(fb.FA_OP_BWD, 1, 300, 4, 2, 64, fb.FA_DTYPE_BF16)
+    full = fb.fa_workspace_size(fb.FA_OP_BWD_FUSED, 1, 300, 4, 2, 64, fb.FA_DTYPE_BF16)
     args = (1, 300, 4, 2)
     call = lambda D, causal, dt, ws_bytes: fb.fa_bwd_dkdv_dq(*p, *args, D, 0.125, causal, 0, dt, FAKE, ws_bytes, None)
     assert call(64, 0, fb.FA_DTYPE_BF16, full) == fb.FA_ERR_UNSUPPORTED   # not causal

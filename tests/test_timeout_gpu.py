@@ -44,15 +44,11 @@ def test_stalled_forward_times_out_and_recovers():
     assert np.max(np.abs(lse.cpu().numpy() - L)) <= 1e-3
 
 
-@pytest.mark.parametrize("kind,bit,D", [(2, 2, 128), (3, 4, 128), (2, 2, 64)], ids=["dkdv", "dq", "fused"])
-def test_stalled_backward_kernel_times_out_and_recovers(kind, bit, D):
-    """The dK/dV kernel and the dQ kernel (head dim 128), and the fused
-    dK/dV + dQ kernel (head dim 64, which takes the dK/dV hook): the stalled
-    kernel gives up, reports only its own bit, and the next backward -- the
-    fused one with its turn counters reset -- is correct."""
+@pytest.mark.parametrize("kind,bit", [(2, 2), (3, 4)], ids=["dkdv", "dq"])
+def test_stalled_backward_kernel_times_out_and_recovers(kind, bit):
     from flash_attention_attn_gb300.build import build
     build()
-    w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, D, 0, True, True, "normal")
+    w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, 64, 0, True, True, "normal")
     inp = make_inputs(w, seed=4)
     dev = torch.device("cuda", 0)
     q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
@@ -81,3 +77,45 @@ def test_stall_hook_rejects_unknown_kinds():
     assert fa.fa_debug_config(0, 4) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_debug_config(0, -1) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_debug_config(0, 0) == fa.FA_OK
+
+
+def test_stalled_fused_backward_times_out_and_recovers():
+    """The fused dK/dV + dQ kernel (fa_bwd_dkdv_dq) takes the dK/dV hook: its
+    waits give up (the turn waits among them), only the dK/dV bit is set, and
+    the next call -- its turn counters cleared again -- is correct."""
+    from flash_attention_attn_gb300.build import build
+    build()
+    w = Workload(202, "timeout-fused", "bf16", 1, 4, 2, 300, 64, 0, True, True, "normal")
+    inp = make_inputs(w, seed=5)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=True)
+    fa.check_status()
+    n = fa.fa_workspace_size(fa.FA_OP_BWD_FUSED, w.B, w.T, w.H, w.HKV, w.D, fa.FA_DTYPE_BF16)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    P = [t.data_ptr() for t in (q, k, v, o, lse, do)]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    args = (w.B, w.T, w.H, w.HKV, w.D, w.scale, 1, 0, fa.FA_DTYPE_BF16, ws.data_ptr(), n, s)
+
+    def run():
+        assert fa.fa_bwd_preprocess(P[3], P[5], w.B, w.T, w.H, w.HKV, w.D, fa.FA_DTYPE_BF16, ws.data_ptr(), n,
+                                    s) == fa.FA_OK
+        assert fa.fa_bwd_dkdv_dq(P[0], P[1], P[2], P[4], P[5], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                 *args) == fa.FA_OK
+        return fa.fa_check_status(ws.data_ptr(), s)
+
+    try:
+        fa.fa_debug_config(200_000_000, 2)
+        st, word = run()
+    finally:
+        fa.fa_debug_config(0, 0)
+    assert st == fa.FA_ERR_TIMEOUT
+    assert word == 2, hex(word)
+    st, word = run()
+    assert st == fa.FA_OK, hex(word)
+    Q, K, V, dO = (as_f64(inp[x]) for x in ("q", "k", "v", "do"))
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, True, 0)
+    for got, ref in ((dq, dQ), (dk, dK), (dv, dV)):
+        g = got.float().cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(g - ref) / np.linalg.norm(ref) <= 2e-2
