@@ -265,7 +265,7 @@ int bwd_maps(fa::TensorMaps* tm, const void* Q, const void* K, const void* V, co
 
 fa::BwdParams bwd_params(const Shape& s, const float* LSE, const float* delta, void* dQ, void* dK, void* dV,
                          void* workspace, int dtype, int stall_kind) {
-  fa::BwdParams p;
+  fa::BwdParams p{};
   int dev = 0;
   cudaGetDevice(&dev);  // already checked by bwd_prologue
   p.ctas = persistent_ctas(dev);
@@ -316,7 +316,7 @@ int dkdv_impl(const void* Q, const void* K, const void* V, const float* LSE, con
 
 int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const void* dO, void* dQ, int B, int T,
             int Tk, int H, int HKV, int head_dim, float scale, int causal, int window, int dtype, void* workspace,
-            size_t workspace_bytes, void* stream) {
+            size_t workspace_bytes, void* stream, bool after_dkdv = false) {
   const void* ptrs[] = {Q, K, V, LSE, dO, dQ};
   Shape shp;
   float* delta;
@@ -330,7 +330,9 @@ int dq_impl(const void* Q, const void* K, const void* V, const float* LSE, const
                                             static_cast<float*>(dQ), shp, s));
   fa::TensorMaps tm;
   if ((st = bwd_maps(&tm, Q, K, V, dO, shp, dtype)) != FA_OK) return st;
-  return status_of(fa::launch_bwd_dq_bf16(tm, bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype, 3), s));
+  fa::BwdParams p = bwd_params(shp, LSE, delta, dQ, nullptr, nullptr, workspace, dtype, 3);
+  p.after_dkdv = after_dkdv ? 1 : 0;
+  return status_of(fa::launch_bwd_dq_bf16(tm, p, s));
 }
 
 // 4-D fp32 view [B][T][heads][D] of the dQ accumulator; boxes of 32
@@ -405,8 +407,10 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const f
   if ((st = dkdv_impl(Q, K, V, LSE, dO, dK, dV, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
                       workspace_bytes, stream)) != FA_OK)
     return st;
+  // dQ reads nothing that dK/dV writes: its CTAs may start on the SMs that
+  // the dK/dV kernel leaves idle (fewer units than SMs, or its tail)
   return dq_impl(Q, K, V, LSE, dO, dQ, B, T, Tk, H, HKV, head_dim, scale, causal, window, dtype, workspace,
-                 workspace_bytes, stream);
+                 workspace_bytes, stream, /*after_dkdv=*/true);
 }
 
 }  // namespace

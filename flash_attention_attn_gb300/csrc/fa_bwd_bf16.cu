@@ -224,6 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = DkdvTiles<D>;
   constexpr int BQ = 128;  // query rows per streamed block
   constexpr int BK = 128;  // key rows per unit
+  // the dQ kernel that follows inside one backward call reads nothing this
+  // kernel writes: let its CTAs take the SMs this grid leaves idle
+  grid_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::kSlack)) {
@@ -907,6 +910,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // launched as a dependent of the dK/dV kernel, this grid may not complete
+  // before that one: work after the backward on the stream sees dK and dV
+  if (threadIdx.x == 0) grid_dependency_wait();
 }
 
 template <int D, bool F16>
@@ -934,9 +940,17 @@ cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t s
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const dim3 grid(imax(1, imin(p.ctas, dq_units(p.s))));
-  fa_bwd_dq_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(imax(1, imin(p.ctas, dq_units(p.s))));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.after_dkdv ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fa_bwd_dq_bf16_kernel<D, F16>, tm.q, tm.k, tm.v, tm.dO, p);
 }
 
 }  // namespace

@@ -113,6 +113,7 @@ struct BwdParams {
   SchedCounter* sched;  // persistent kernels: their work counter in the workspace (zero between launches)
   float* dq_acc;        // fused backward: fp32 dQ accumulator [B,T,H,D] (workspace)
   unsigned int* turns;  // fused backward: turn counter per (b, h, query block) (workspace, zero between launches)
+  int after_dkdv;       // dQ: launched as a programmatic dependent of the dK/dV kernel just before it on the stream
 };
 
 // 3-D views [B][T][heads*D] with boxes of 64 elements x R rows x 1 batch:

@@ -118,8 +118,13 @@ int fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * Runs three kernels in stream order: Delta = rowsum(dO * O) into the
  * workspace, then dK/dV (every KV block accumulated privately by one unit of
  * work, no atomics), then dQ (every query block by one unit, fixed order, no
- * atomics), so the result is bitwise reproducible.  (fa_bwd_dkdv_dq is the
- * alternative second stage that forms dQ without recomputing S and dP.)
+ * atomics), so the result is bitwise reproducible.  dQ reads nothing dK/dV
+ * writes, so it is launched as a programmatic dependent of dK/dV (16-bit
+ * types): its CTAs start on the SMs the dK/dV kernel leaves idle, and it
+ * completes only after dK/dV has, so work queued after fa_bwd sees all three
+ * gradients.  The results are the same bits as the three stage calls.
+ * (fa_bwd_dkdv_dq is the alternative second stage that forms dQ without
+ * recomputing S and dP.)
  *   O, LSE: exactly what fa_fwd produced for the same inputs.
  *   workspace >= fa_workspace_size(FA_OP_BWD, ...).
  */

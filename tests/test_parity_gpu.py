@@ -341,6 +341,61 @@ def test_backward_is_bitwise_reproducible(D, window):
         assert torch.equal(a, b) and torch.equal(a, c)
 
 
+OVERLAP_CASES = [
+    # dtype, B, H, HKV, T, D, window, CTA cap (0 = one per SM)
+    ("bf16", 1, 8, 2, 640, 64, 0, 0),      # 10 dK/dV units: most SMs start on dQ at once
+    ("bf16", 2, 8, 4, 4096, 128, 0, 0),    # 256 dK/dV units: dQ fills the dK/dV tail
+    ("fp16", 1, 4, 4, 1000, 128, 300, 3),  # three CTAs each: dQ runs beside all of dK/dV
+    ("bf16", 2, 4, 1, 777, 32, 0, 5),      # ragged tail, head dim 32
+]
+
+
+@pytest.mark.parametrize("case", OVERLAP_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward_call_equals_its_stages(case):
+    """fa_bwd launches dQ as a programmatic dependent of dK/dV, so that dQ
+    CTAs start on the SMs dK/dV leaves idle; the stage entry points launch
+    them one after the other.  Both give the same bits, and work queued after
+    fa_bwd sees its dK and dV (read here right after the call)."""
+    dtype, B, H, HKV, T, D, window, cap = case
+    w = Workload(108, "overlap", dtype, B, H, HKV, T, D, window, True, True, "normal")
+    inp = make_inputs(w, seed=7000 + T + D)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, scale=w.scale, causal=True, window=window)
+    dt = fa.FA_DTYPE_BF16 if dtype == "bf16" else fa.FA_DTYPE_FP16
+    n = fa.fa_workspace_size(fa.FA_OP_BWD, B, T, H, HKV, D, dt)
+    ws = torch.zeros(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    P = [t.data_ptr() for t in (q, k, v, o, lse, do)]
+    args = (B, T, H, HKV, D, w.scale, 1, window, dt, ws.data_ptr(), n, s)
+    outs = {}
+    assert fa.fa_debug_max_ctas(cap) == fa.FA_OK
+    try:
+        for path in ("stages", "fa_bwd", "fa_bwd-again"):
+            dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+            if path == "stages":
+                assert fa.fa_bwd_preprocess(P[3], P[5], B, T, H, HKV, D, dt, ws.data_ptr(), n, s) == fa.FA_OK
+                assert fa.fa_bwd_dkdv(P[0], P[1], P[2], P[4], P[5], dk.data_ptr(), dv.data_ptr(), *args) == fa.FA_OK
+                assert fa.fa_bwd_dq(P[0], P[1], P[2], P[4], P[5], dq.data_ptr(), *args) == fa.FA_OK
+            else:
+                assert fa.fa_bwd(*P, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), *args) == fa.FA_OK
+            # consumers on the same stream, queued before any host synchronisation
+            outs[path] = tuple(t.clone() for t in (dq, dk, dv))
+            st, word = fa.fa_check_status(ws.data_ptr(), s)
+            assert st == fa.FA_OK, hex(word)
+    finally:
+        fa.fa_debug_max_ctas(0)
+    for path in ("fa_bwd", "fa_bwd-again"):
+        for name, a, b in zip(("dQ", "dK", "dV"), outs["stages"], outs[path]):
+            assert torch.equal(a, b), (path, name)
+    if T > 1024:
+        return  # the stage path is checked against the oracle at these sizes elsewhere
+    Q, K, V, dO = (as_f64(inp[x]) for x in ("q", "k", "v", "do"))
+    dQ, dK, dV, _ = oracle.bwd(Q, K, V, dO, w.scale, True, window)
+    for name, got, ref in zip(("dQ", "dK", "dV"), outs["fa_bwd"], (dQ, dK, dV)):
+        check_grad(w, name, got.float().cpu().numpy().astype(np.float64), ref)
+
+
 FUSED_CASES = [
     # dtype, B, H, HKV, T, D, window
     ("bf16", 2, 4, 2, 300, 64, 0),     # ragged tail, GQA
