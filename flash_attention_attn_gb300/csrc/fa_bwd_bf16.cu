@@ -80,9 +80,11 @@ __device__ __forceinline__ void load_two_cols32(uint32_t a0, uint32_t a1, float 
 // to global memory at dst (16-byte aligned, ncols a multiple of 32).
 // ncols accumulator columns of this thread's lane, scaled, as 16-bit values;
 // only the first nvalid columns are stored (a head dim below the kernel's).
+// st32: dst is 32-byte aligned and nvalid a multiple of 16, so the row
+// leaves in whole 32-byte sectors.
 template <bool F16>
 __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, int nvalid, float mul, uint16_t* dst,
-                                              bool valid) {
+                                              bool valid, bool st32) {
   for (int c = 0; c < ncols; c += 32) {
     uint32_t r[32];
     tmem_ld32(taddr + c, r);
@@ -92,10 +94,16 @@ __device__ __forceinline__ void store_acc_row(uint32_t taddr, int ncols, int nva
     for (int e = 0; e < 16; ++e)
       pk[e] = pack2<F16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
     if (valid) {
-      uint4* d = reinterpret_cast<uint4*>(dst + c);
+      if (st32) {
 #pragma unroll
-      for (int v = 0; v < 4; ++v)
-        if (c + v * 8 < nvalid) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 2; ++v)
+          if (c + v * 16 < nvalid) st_global_v8(dst + c + v * 16, pk + 8 * v);
+      } else {
+        uint4* d = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          if (c + v * 8 < nvalid) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+      }
     }
   }
 }
@@ -580,10 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(w.b) * s.Tk + j) * s.HKV + w.g) * s.D + half * (D / 2);
       const int nvalid = s.D - half * (D / 2);  // columns of this half inside the head dim
+      const bool st32 =
+          ((reinterpret_cast<uintptr_t>(p.dK) | reinterpret_cast<uintptr_t>(p.dV)) & 31) == 0 && (s.D & 15) == 0;
       store_acc_row<F16>(tmem + lane_addr + C::kTmDV + half * (D / 2), D / 2, nvalid, 1.f,
-                         static_cast<uint16_t*>(p.dV) + rowoff, j < s.Tk);
+                         static_cast<uint16_t*>(p.dV) + rowoff, j < s.Tk, st32);
       store_acc_row<F16>(tmem + lane_addr + C::kTmDK + half * (D / 2), D / 2, nvalid, s.scale,
-                         static_cast<uint16_t*>(p.dK) + rowoff, j < s.Tk);
+                         static_cast<uint16_t*>(p.dK) + rowoff, j < s.Tk, st32);
     }
   }
 
@@ -897,8 +907,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++uc;
       tc_fence_after();
       const size_t rowoff = ((static_cast<size_t>(w.b) * s.T + i) * s.H + w.h) * s.D + half * (D / 2);
+      const bool st32 = (reinterpret_cast<uintptr_t>(p.dQ) & 31) == 0 && (s.D & 15) == 0;
       store_acc_row<F16>(tmem + lane_addr + C::kTmDQ + half * (D / 2), D / 2, s.D - half * (D / 2), s.scale,
-                         static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T);
+                         static_cast<uint16_t*>(p.dQ) + rowoff, i < s.T, st32);
     }
   }
 

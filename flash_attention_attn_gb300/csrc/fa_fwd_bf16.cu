@@ -551,13 +551,23 @@ __global__ void __launch_bounds__(kThreads2, 1)
         if (u >= nunits) break;  // the end marker has been handed on
         const Fwd2Unit w = fwd2_unit(s, pack, u);
         // Q_A, Q_B of this unit once the previous unit's score MMAs are done
-        if (uc > 0 && !(ok = warp_wait(&bars->q_empty, (uc - 1) & 1, ctl, kCode))) break;
-        mbar_arrive_expect_tx_e(&bars->q_full, (w.has_b ? 2 : 1) * C::kTileBytes);
-        for (int t = 0; t < (w.has_b ? 2 : 1); ++t)
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64,
-                          t ? w.h_b : w.h_a, (t ? w.q_b : w.q_a) * kBM, w.b);
-        ++uc;
+        auto load_q = [&]() -> bool {
+          if (uc > 0 && !warp_wait(&bars->q_empty, (uc - 1) & 1, ctl, kCode)) return false;
+          mbar_arrive_expect_tx_e(&bars->q_full, (w.has_b ? 2 : 1) * C::kTileBytes);
+          for (int t = 0; t < (w.has_b ? 2 : 1); ++t)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d_e(&tmQ, &bars->q_full, smem + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, c * 64,
+                            t ? w.h_b : w.h_a, (t ? w.q_b : w.q_a) * kBM, w.b);
+          ++uc;
+          return true;
+        };
+        // With the two-stage K ring (D = 128) the unit's first K block is
+        // issued before Q: its slot frees before Q's buffer (the previous
+        // unit's last score MMAs), so its latency overlaps that wait (the
+        // windowed workload's forward 0.8 % faster); with the four-stage ring
+        // (D = 64) that order measured 2 % slower.
+        constexpr bool kKFirst = (C::kKStages == 2);
+        if ((!kKFirst || w.nblk == 0) && !(ok = load_q())) break;
         for (int n = 0; n < w.nblk; ++n) {
           const int st = kc % C::kKStages;
           if (kc >= C::kKStages && !(ok = warp_wait(&bars->k_empty[st], ((kc / C::kKStages) - 1) & 1, ctl, kCode)))
@@ -567,6 +577,7 @@ __global__ void __launch_bounds__(kThreads2, 1)
             tma_load_4d_e(&tmK, &bars->k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
                           c * 64, w.g, (w.lo + n) * kBN, w.b);
           ++kc;
+          if (kKFirst && n == 0 && !(ok = load_q())) break;
           const int sv = vc % C::kVStages;
           if (vc >= C::kVStages && !(ok = warp_wait(&bars->v_empty[sv], ((vc / C::kVStages) - 1) & 1, ctl, kCode)))
             break;
@@ -686,6 +697,8 @@ __global__ void __launch_bounds__(kThreads2, 1)
     const uint32_t s_addr = tmem + lane_addr + C::kTmS + t * 128;
     const uint32_t o_addr = tmem + lane_addr + C::kTmO + t * D;
     const float sl2 = p.scale_log2;
+    // O rows start on 32-byte boundaries: whole-sector stores
+    const bool o32 = (reinterpret_cast<uintptr_t>(p.O) & 31) == 0 && (s.D & 15) == 0;
     int sc = 0, oc = 0;  // s_full and o_done phases this tile has waited for
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
@@ -811,20 +824,31 @@ __global__ void __launch_bounds__(kThreads2, 1)
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint16_t* orow = static_cast<uint16_t*>(p.O) + ((static_cast<size_t>(w.b) * s.T + row) * s.H + h) * s.D;
+      // the whole O row in one TMEM round trip (the scores' registers are
+      // free again), so that the next unit's softmax starts sooner
+      uint32_t ro[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(o_addr + c * 32, ro[c]);
+      tmem_ld_wait(ro[0]);
+#pragma unroll
+      for (int c = 1; c < D / 32; ++c) reg_tie(ro[c]);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t ro[32];
-        tmem_ld32(o_addr + c * 32, ro);
-        tmem_ld_wait(ro);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          pk[e] = pack2<F16>(__uint_as_float(ro[2 * e]) * inv, __uint_as_float(ro[2 * e + 1]) * inv);
+          pk[e] = pack2<F16>(__uint_as_float(ro[c][2 * e]) * inv, __uint_as_float(ro[c][2 * e + 1]) * inv);
         if (row < s.T) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          if (o32) {  // 32-byte stores: one whole sector per store
 #pragma unroll
-          for (int v = 0; v < 4; ++v)  // columns past a head dim below D are not stored
-            if (c * 32 + v * 8 < s.D) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < 2; ++v)
+              if (c * 32 + v * 16 < s.D) st_global_v8(orow + c * 32 + v * 16, pk + 8 * v);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)  // columns past a head dim below D are not stored
+              if (c * 32 + v * 8 < s.D) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
         }
       }
       if (row < s.T) {
