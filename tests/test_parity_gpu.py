@@ -472,6 +472,39 @@ def test_every_output_element_is_written():
         assert torch.isfinite(t).all()
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_outputs_at_16_byte_offsets(D):
+    """Outputs whose rows start 16 but not 32 bytes into a sector take the
+    16-byte store path (32-byte aligned outputs leave in whole sectors): the
+    same kernels' arithmetic, so the same bits, and nothing written outside
+    the views."""
+    w = Workload(109, "offset", "bf16", 2, 4, 2, 300, D, 0, True, True, "normal")
+    inp = make_inputs(w, seed=11)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+
+    def shifted(t):  # a view 8 elements (16 bytes) into a larger NaN-filled buffer
+        buf = torch.full((t.numel() + 16,), float("nan"), dtype=t.dtype, device=dev)
+        view = buf[8:8 + t.numel()].view(t.shape)
+        assert view.data_ptr() % 32 == 16
+        return buf, view
+
+    o_ref, lse_ref = fa.attention_fwd(q, k, v, causal=True)
+    g_ref = fa.attention_bwd(q, k, v, o_ref, lse_ref, do, causal=True)
+    ob, o = shifted(q)
+    lse = torch.empty_like(lse_ref)
+    fa.attention_fwd(q, k, v, causal=True, out=o, lse=lse)
+    bufs = [shifted(t) for t in (q, k, v)]
+    fa.attention_bwd(q, k, v, o, lse, do, causal=True, dq=bufs[0][1], dk=bufs[1][1], dv=bufs[2][1])
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, hex(word)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    for (buf, view), ref in zip(bufs, g_ref):
+        assert torch.equal(view, ref)
+    for buf in (ob, *(b for b, _ in bufs)):  # the 8 elements either side stay NaN
+        assert torch.isnan(buf[:8]).all() and torch.isnan(buf[-8:]).all()
+
+
 # ----------------------------------------- named workloads, full size, sampled
 
 def _sample_rows(T, rng, n_random):
