@@ -347,9 +347,14 @@ def attention_fwd(q, k, v, scale=None, causal=True, window=0, out=None, lse=None
 
 
 def attention_bwd(q, k, v, o, lse, do, scale=None, causal=True, window=0, dq=None, dk=None, dv=None,
-                  stream=None):
+                  stream=None, recompute_dq=True):
     """dQ, dK, dV given the forward's O and LSE and the output gradient dO
-    (cross-attention when k and v are longer or shorter than q)."""
+    (cross-attention when k and v are longer or shorter than q).
+
+    recompute_dq=False runs fa_bwd_preprocess + fa_bwd_dkdv_dq: dQ from the
+    dK/dV pass's dS tiles, summed in a fixed order, without recomputing S
+    and dP (16-bit types, head dims up to 64, causal masking; slower than the
+    default on GB300, see include/fa.h)."""
     torch = _torch()
     B, T, H, D = q.shape
     Tk, HKV = k.shape[1], k.shape[2]
@@ -367,6 +372,20 @@ def attention_bwd(q, k, v, o, lse, do, scale=None, causal=True, window=0, dq=Non
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     s = _stream(dev, stream)
+    if not recompute_dq:
+        if Tk != T or not causal or fa_workspace_size(FA_OP_BWD_FUSED, B, T, H, HKV, D, dt) == 0:
+            raise FaError(FA_ERR_UNSUPPORTED, "attention_bwd: recompute_dq=False needs causal self-attention "
+                                              "with 16-bit elements and a head dim of at most 64")
+        ws, n = workspace(FA_OP_BWD_FUSED, B, T, H, HKV, D, dt, dev, s)
+        st = fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), B, T, H, HKV, D, dt, ws.data_ptr(), n, s)
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_preprocess")
+        st = fa_bwd_dkdv_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), lse.data_ptr(), do.data_ptr(), dq.data_ptr(),
+                            dk.data_ptr(), dv.data_ptr(), B, T, H, HKV, D, float(scale), 1, int(window), dt,
+                            ws.data_ptr(), n, s)
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_dkdv_dq")
+        return dq, dk, dv
     ws, n = workspace(FA_OP_BWD, B, T, H, HKV, D, dt, dev, s)
     if Tk != T:
         st = fa_bwd_cross(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),

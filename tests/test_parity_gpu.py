@@ -456,6 +456,35 @@ def test_fused_backward_against_separate_kernels_and_oracle(case):
         check_grad(w, f"dQ ({path})", outs[path][0].float().cpu().numpy().astype(np.float64), dQ)
 
 
+def test_attention_bwd_without_dq_recompute():
+    """attention_bwd(recompute_dq=False) is the fused stage: dK and dV the
+    same bits as the default path, dQ within the parity tolerance of the
+    oracle and the same bits on a second call; shapes it does not cover are
+    refused before any launch."""
+    w = Workload(110, "fused-api", "bf16", 2, 4, 2, 520, 64, 200, True, True, "normal")
+    inp = make_inputs(w, seed=12)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    o, lse = fa.attention_fwd(q, k, v, causal=True, window=w.window)
+    ref = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=w.window)
+    g1 = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=w.window, recompute_dq=False)
+    g2 = fa.attention_bwd(q, k, v, o, lse, do, causal=True, window=w.window, recompute_dq=False)
+    st, word = fa.check_status()
+    assert st == fa.FA_OK, hex(word)
+    assert torch.equal(g1[1], ref[1]) and torch.equal(g1[2], ref[2])
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+    Q, K, V, dO = (as_f64(inp[x]) for x in ("q", "k", "v", "do"))
+    dQ, _, _, _ = oracle.bwd(Q, K, V, dO, w.scale, True, w.window)
+    check_grad(w, "dQ", g1[0].float().cpu().numpy().astype(np.float64), dQ)
+    q128 = torch.zeros(1, 128, 2, 128, dtype=torch.bfloat16, device=dev)
+    o128, lse128 = fa.attention_fwd(q128, q128, q128, causal=True)
+    with pytest.raises(fa.FaError):
+        fa.attention_bwd(q128, q128, q128, o128, lse128, q128, causal=True, recompute_dq=False)
+    with pytest.raises(fa.FaError):
+        fa.attention_bwd(q, k, v, o, lse, do, causal=False, recompute_dq=False)
+
+
 def test_every_output_element_is_written():
     w = Workload(102, "poison", "bf16", 2, 4, 2, 333, 64, 0, True, True, "normal")
     inp = make_inputs(w, seed=9)
