@@ -929,13 +929,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool F16>
 cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
   using C = DkdvTiles<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  const void* kfn = reinterpret_cast<const void*>(fa_bwd_dkdv_bf16_kernel<D, F16>);
+  if (cudaError_t e = set_smem_once(kfn, C::kSmemBytes, attr_set); e != cudaSuccess) return e;
   const dim3 grid(imax(1, imin(p.ctas, dkdv_units(p.s))));
   fa_bwd_dkdv_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, tm.dO, p);
   return cudaGetLastError();
@@ -944,13 +940,9 @@ cudaError_t launch_dkdv_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t
 template <int D, bool F16>
 cudaError_t launch_dq_d(const TensorMaps& tm, const BwdParams& p, cudaStream_t stream) {
   using C = DqTiles<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  const void* kfn = reinterpret_cast<const void*>(fa_bwd_dq_bf16_kernel<D, F16>);
+  if (cudaError_t e = set_smem_once(kfn, C::kSmemBytes, attr_set); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(imax(1, imin(p.ctas, dq_units(p.s))));
   cfg.blockDim = dim3(kThreads);

@@ -650,17 +650,13 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 
 template <bool F16>
 cudaError_t launch_fused(const TensorMaps& tm, const CUtensorMap& acc_map, const BwdParams& p, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_bwd_fused_d64_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         FusedTiles::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // the cooperative launch checks residency against the preferred carveout
-    e = cudaFuncSetAttribute(fa_bwd_fused_d64_kernel<F16>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  // the cooperative launch checks residency against the preferred carveout:
+  // raise it too
+  static std::atomic<unsigned long long> attr_set{0};
+  if (cudaError_t e = set_smem_once(reinterpret_cast<const void*>(fa_bwd_fused_d64_kernel<F16>),
+                                    FusedTiles::kSmemBytes, attr_set, /*carveout=*/true);
+      e != cudaSuccess)
+    return e;
   const int units = fused_units(p.s);
   // cooperative: every CTA is resident at once, so every unit a turn waits
   // for is running or done

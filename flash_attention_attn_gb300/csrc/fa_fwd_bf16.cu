@@ -871,13 +871,9 @@ __global__ void __launch_bounds__(kThreads2, 1)
 template <int D, bool F16>
 cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   using C = Fwd2Cfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd2_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  const void* kfn = reinterpret_cast<const void*>(fa_fwd2_bf16_kernel<D, F16>);
+  if (cudaError_t e = set_smem_once(kfn, C::kSmemBytes, attr_set); e != cudaSuccess) return e;
   const int units = fwd2_units(p.s, p.pack_heads != 0);
   const dim3 grid(imax(1, imin(p.ctas, units)));
   fa_fwd2_bf16_kernel<D, F16><<<grid, kThreads2, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
@@ -887,13 +883,9 @@ cudaError_t launch_fwd2_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t
 template <int D, bool F16>
 cudaError_t launch_fwd_d(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fa_fwd_bf16_kernel<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};
+  const void* kfn = reinterpret_cast<const void*>(fa_fwd_bf16_kernel<D, F16>);
+  if (cudaError_t e = set_smem_once(kfn, C::kSmemBytes, attr_set); e != cudaSuccess) return e;
   dim3 grid(ceil_div(p.s.T, kBM), p.s.H, p.s.B);
   fa_fwd_bf16_kernel<D, F16><<<grid, kThreads, C::kSmemBytes, stream>>>(tm.q, tm.k, tm.v, p);
   return cudaGetLastError();

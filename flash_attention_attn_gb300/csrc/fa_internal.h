@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace fa {
 
 // Query rows per tile and key rows per block of the bf16 tensor-core kernels.
@@ -121,6 +123,24 @@ struct BwdParams {
 struct TensorMaps {
   CUtensorMap q, k, v, dO;
 };
+
+// Raises a kernel's dynamic shared-memory limit (and, with carveout, its
+// preferred carveout to the maximum) once per device: the attribute belongs
+// to the kernel's instance on the current device.  `done` holds one bit per
+// device ordinal.
+inline cudaError_t set_smem_once(const void* kernel, int bytes, std::atomic<unsigned long long>& done,
+                                 bool carveout = false) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && carveout)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 cudaError_t launch_fwd_bf16(const TensorMaps& tm, const FwdParams& p, cudaStream_t stream);
 // Pre-attention prologue (RMS-norm + rotary of the packed QK projection).
