@@ -1,11 +1,13 @@
 // fa_bwd_bf16.cu -- attention backward for sm_103a (tcgen05 + TMA).
 //
-// Two kernels, each recomputing P block by block from the forward's LSE:
+// Two kernels, each recomputing P block by block from the forward's LSE.
+// Both are persistent (at most one CTA per SM, units of work handed out
+// longest first, fa_sched.cuh):
 //
-// dK/dV: one CTA per (b, kv head g, 128-row KV block).  K and V stay in
-//   shared memory and dK, dV in TMEM for the CTA's whole life while it visits
+// dK/dV: a unit is (b, kv head g, 128-row KV block).  K and V stay in
+//   shared memory and dK, dV in TMEM for the whole unit while it visits
 //   every query head of the group and every 128-row query block that sees the
-//   KV block.  Accumulation is private to the CTA: no atomics.
+//   KV block.  Accumulation is private to the unit: no atomics.
 //     S^T  = K Q^T          (TMEM, KV rows on lanes)
 //     dP^T = V dO^T
 //     P^T  = 2^(S^T*scale*log2e - LSE*log2e), masked           -> bf16, TMEM
@@ -16,8 +18,8 @@
 //   the group's query heads; teeny-kernels flash_attn2.rs,
 //   flash_attention2_backward_dkv: no atomics are needed.)
 //
-// dQ: one CTA per (b, h, 128-row query block); loops over the visible 128-row
-//   KV blocks in a fixed order, so the result is bitwise reproducible.
+// dQ: a unit is (b, h, 128-row query block); it loops over the visible
+//   128-row KV blocks in a fixed order, so the result is bitwise reproducible.
 //     S = Q K^T ; dP = dO V^T ; dS = P (dP - Delta) -> bf16, TMEM ; dQ += dS K
 //   and at the end dQ *= scale.  (forge flash_attention.metal,
 //   flash_attn_bwd_dq; teeny-kernels flash_attention2_backward_dq.)

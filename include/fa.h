@@ -134,13 +134,15 @@ int fa_bwd(const void* Q, const void* K, const void* V, const void* O, const flo
            int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The three stages of fa_bwd, callable one by one (fa_bwd runs exactly these
- * launches, in this order, on `stream`).  Same arguments and layouts as
+ * The three stages of fa_bwd, callable one by one (fa_bwd runs these kernels
+ * in this order on `stream`, the dQ one as a programmatic dependent of the
+ * dK/dV one; called one by one they run in plain stream order, with the same
+ * results bit for bit).  Same arguments and layouts as
  * fa_bwd; the workspace carries Delta from the first stage to the other two,
  * so all three must get the same workspace and be stream-ordered.
  *   fa_bwd_preprocess: Delta = rowsum(dO * O) into the workspace (HBM-bound).
- *   fa_bwd_dkdv:       dK, dV (one CTA per KV block, no atomics).
- *   fa_bwd_dq:         dQ (one CTA per query block, fixed order, no atomics).
+ *   fa_bwd_dkdv:       dK, dV (one unit of work per KV block, no atomics).
+ *   fa_bwd_dq:         dQ (one unit of work per query block, fixed order, no atomics).
  */
 int fa_bwd_preprocess(const void* O, const void* dO, int B, int T, int H, int HKV, int head_dim, int dtype,
                       void* workspace, size_t workspace_bytes, void* stream);
