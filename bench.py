@@ -522,7 +522,10 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
     o = torch.empty_like(q)
     lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = fb.fa_workspace_size(fb.FA_OP_BWD, B, T, H, HKV, D, dt)
+    fused = bool(args.fused_bwd) and fused_backward(w)
+    if args.fused_bwd and not fused:
+        raise SystemExit("--fused-bwd needs a causal 16-bit workload with a head dim of at most 64")
+    ws_bytes = fb.fa_workspace_size(fb.FA_OP_BWD_FUSED if fused else fb.FA_OP_BWD, B, T, H, HKV, D, dt)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     s = stream.cuda_stream
@@ -553,7 +556,9 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
         check(lib.fa_bwd_dkdv_dq(P[0], P[1], P[2], P[4], P[5], P[6], P[7], P[8], B, T, H, HKV, D, sc, causal, win,
                                  dt, wsp, ws_bytes, s), "fa_bwd_dkdv_dq")
 
-    kernels = ["fwd"] + backward_stages(w)
+    # the step: fa_fwd and fa_bwd's three stages, or with --fused-bwd the
+    # opt-in second stage that forms dQ without recomputing S and dP
+    kernels = ["fwd"] + (["bwd_preprocess", "bwd_dkdv_dq"] if fused else backward_stages(w))
     by_name = {"fwd": k_fwd, "bwd_preprocess": k_pre, "bwd_dkdv": k_dkdv, "bwd_dq": k_dq, "bwd_dkdv_dq": k_fused}
     stages = tuple(by_name[n] for n in kernels)
     in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do))
@@ -608,6 +613,11 @@ def run_ours(args, w: Workload, world: int, rank: int, local: int) -> dict:
         def run_set(bs):  # the public calls: fa_fwd, then fa_bwd
             qq, kk, vv, dd, oo, ll, gq, gk, gv = (t.data_ptr() for t in bs)
             check(lib.fa_fwd(qq, kk, vv, oo, ll, B, T, H, HKV, D, sc, causal, win, dt, wsp, ws_bytes, s), "fa_fwd")
+            if fused:
+                check(lib.fa_bwd_preprocess(oo, dd, B, T, H, HKV, D, dt, wsp, ws_bytes, s), "fa_bwd_preprocess")
+                check(lib.fa_bwd_dkdv_dq(qq, kk, vv, ll, dd, gq, gk, gv, B, T, H, HKV, D, sc, causal, win, dt, wsp,
+                                         ws_bytes, s), "fa_bwd_dkdv_dq")
+                return
             check(lib.fa_bwd(qq, kk, vv, oo, ll, dd, gq, gk, gv, B, T, H, HKV, D, sc, causal, win, dt, wsp,
                              ws_bytes, s), "fa_bwd")
 
@@ -726,6 +736,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue", action="store_true", help="skip the QK-norm + rotary prologue measurement")
     ap.add_argument("--no-workloads", action="store_true", help="skip the other configurations' loops")
+    ap.add_argument("--fused-bwd", action="store_true",
+                    help="step with the opt-in fused backward stage (causal 16-bit, head dim <= 64)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.shape:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -830,6 +842,8 @@ def main():
                        "seconds-long loop under the power cap, _of_nominal against NVIDIA's published dense rate",
         "roofline": roof,
         "kernels": kern,
+        "backward": ("fa_bwd_preprocess + fa_bwd_dkdv_dq (opt-in fused stage)" if "bwd_dkdv_dq" in r["kernels"]
+                     else "fa_bwd: fa_bwd_preprocess + fa_bwd_dkdv + fa_bwd_dq"),
         "gpu_launches": len(r["kernels"]) * args.steps,
         "clocks": r["clocks"],
         "e2e": r["e2e"],
