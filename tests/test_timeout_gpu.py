@@ -44,8 +44,12 @@ def test_stalled_forward_times_out_and_recovers():
     assert np.max(np.abs(lse.cpu().numpy() - L)) <= 1e-3
 
 
+@pytest.mark.parametrize("ctas", [0, 3], ids=["all-sms", "3-ctas"])
 @pytest.mark.parametrize("kind,bit", [(2, 2), (3, 4)], ids=["dkdv", "dq"])
-def test_stalled_backward_kernel_times_out_and_recovers(kind, bit):
+def test_stalled_backward_kernel_times_out_and_recovers(kind, bit, ctas):
+    """With every SM or with three CTAs (each aborting CTA still counts
+    itself out of the persistent scheduler, so the work counters are zero
+    again for the next call, which the oracle check below would notice)."""
     from flash_attention_attn_gb300.build import build
     build()
     w = Workload(201, "timeout-bwd", "bf16", 1, 4, 2, 300, 64, 0, True, True, "normal")
@@ -56,10 +60,12 @@ def test_stalled_backward_kernel_times_out_and_recovers(kind, bit):
     fa.check_status()
     try:
         fa.fa_debug_config(200_000_000, kind)
+        assert fa.fa_debug_max_ctas(ctas) == fa.FA_OK
         fa.attention_bwd(q, k, v, o, lse, do, causal=True)
         st, word = fa.check_status()
     finally:
         fa.fa_debug_config(0, 0)
+        fa.fa_debug_max_ctas(0)
     assert st == fa.FA_ERR_TIMEOUT
     assert word & bit and not word & ~bit & 7, hex(word)  # only the stalled kernel reports
     # the context still works and the next backward is correct
