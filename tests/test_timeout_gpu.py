@@ -19,7 +19,8 @@ from flash_attention_attn_gb300.inputs import Workload, as_f64, make_inputs
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_forward_times_out_and_recovers():
+@pytest.mark.parametrize("ctas", [0, 1], ids=["all-sms", "1-cta"])
+def test_stalled_forward_times_out_and_recovers(ctas):
     from flash_attention_attn_gb300.build import build
     build()
     w = Workload(200, "timeout", "bf16", 1, 2, 2, 256, 64, 0, True, False, "normal")
@@ -29,10 +30,12 @@ def test_stalled_forward_times_out_and_recovers():
     fa.check_status()  # clear anything earlier tests left
     try:
         fa.fa_debug_config(200_000_000, 1)
+        assert fa.fa_debug_max_ctas(ctas) == fa.FA_OK
         fa.attention_fwd(q, k, v, causal=True)
         st, word = fa.check_status()
     finally:
         fa.fa_debug_config(0, 0)
+        fa.fa_debug_max_ctas(0)
     assert st == fa.FA_ERR_TIMEOUT
     assert word & 1  # FA_DEVERR_FWD_TIMEOUT
     # the context still works and the next call is correct
